@@ -1,0 +1,177 @@
+"""EasySpec speculative decoding loop (oracle side), one sequence at a time.
+
+TEST INFRASTRUCTURE ONLY -- see the package docstring.
+
+Stage order per drafting-and-verification iteration follows the method's
+description (arXiv abstract page; OpenReview discussion page, reply on
+Figure 2): fuzzy drafting of N (= gamma) tokens, verification by the base
+model in one forward, then calibration of the draft model's KV cache in a
+single forward pass, which replaces the fuzzy entries so their effect never
+outlives one drafting phase.
+
+State of one sequence (``Row``):
+  tokens      committed tokens x_0..x_{n-1} (prompt + output so far)
+  base cache  exact K/V for positions 0..n-2; x_{n-1} is pending for the base
+  draft cache exact K/V for positions 0..draft_len-1; tokens from draft_len on
+              are pending calibration (their cached K/V, if any, are fuzzy)
+
+Readings (the pages leave these steps open; see also the design notes):
+  * Calibration is merged with the next phase's first draft forward: the
+    exact draft forward over the pending tokens [accepted drafts..., bonus]
+    rewrites their K/V and its last row gives q_1, from which d_1 is drawn.
+    A phase therefore runs gamma draft forwards: one exact multi-token
+    calibration forward and gamma-1 fuzzy single-token forwards.
+  * The fuzzy positions of a phase are those of d_1..d_{gamma-1}; d_gamma is
+    never a draft input within its phase.
+  * The base verifies [x_{n-1}, d_1..d_gamma] at positions n-1..n+gamma-1 and
+    yields p_1..p_{gamma+1}.
+  * After acceptance of a tokens and the bonus/resampled y: tokens grow by
+    a+1, the base keeps positions up to n+a-1 (y pending), the draft keeps
+    exact positions up to n-1 and [d_1..d_a, y] become its pending tokens.
+  * The prompt's base prefill covers x_0..x_{P-2}; the draft's prompt
+    prefill is the first calibration.
+  * Every phase drafts a full gamma; the output is cut to max_new at the end.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import model as M
+from .rng import phase_draws
+from .sampling import accept_resample, argmax_f32, draft_token, softmax_f32
+
+
+def _dist(z64, temperature: float):
+    """float32 logits (greedy) or float32 probabilities softmax(z/T)."""
+    z = np.asarray(z64, dtype=np.float32)
+    if temperature == 0.0:
+        return z
+    return softmax_f32(z, temperature)
+
+
+class Row:
+    def __init__(self, shape_d: M.Shape, shape_b: M.Shape, max_len: int):
+        self.tokens: list[int] = []
+        self.base = M.KVCache(shape_b, max_len)
+        self.draft = M.KVCache(shape_d, max_len)
+        self.draft_len = 0
+        self.phase = 0
+        # per-phase records (for parity checks against the CUDA path)
+        self.q = None      # [gamma, V] float32 draft distributions (or logits)
+        self.p = None      # [gamma+1, V] float32 base distributions (or logits)
+        self.d = None      # [gamma] draft tokens
+        self.zq = None     # [gamma, V] float64 draft logits
+        self.zp = None     # [gamma+1, V] float64 base logits
+        self.n_acc = None
+
+
+class SpecDecoder:
+    """EasySpec loop for a batch of independent rows (row index = RNG row)."""
+
+    def __init__(self, Wd, shape_d: M.Shape, Wb, shape_b: M.Shape,
+                 groups=None, k: int = 1, mode: int = M.FULL_LAYER,
+                 max_len: int = 256):
+        if shape_d.vocab != shape_b.vocab:
+            raise ValueError("draft and base must share one vocabulary")
+        self.Wd, self.sd, self.Wb, self.sb = Wd, shape_d, Wb, shape_b
+        self.groups = groups if groups is not None else M.default_groups(shape_d.n_layers, k)
+        M.check_groups(self.groups, shape_d.n_layers)
+        self.mode = mode
+        self.max_len = max_len
+        self.rows: list[Row] = []
+
+    # -------------------------------------------------------------- stages
+    def prefill(self, prompts):
+        self.rows = []
+        for prompt in prompts:
+            r = Row(self.sd, self.sb, self.max_len)
+            r.tokens = [int(t) for t in prompt]
+            for pos in range(len(r.tokens) - 1):
+                M.forward_exact(self.Wb, self.sb, r.tokens[pos], pos, r.base)
+            self.rows.append(r)
+
+    def calibrate_row(self, r: Row):
+        """Exact draft forward over pending tokens; returns last row's logits."""
+        z = None
+        for pos in range(r.draft_len, len(r.tokens)):
+            z = M.forward_exact(self.Wd, self.sd, r.tokens[pos], pos, r.draft)
+        r.draft_len = len(r.tokens)
+        return z
+
+    def draft_row(self, b: int, gamma: int, temperature: float, seed: int):
+        r = self.rows[b]
+        greedy = temperature == 0.0
+        draws = None if greedy else phase_draws(seed, b, r.phase, gamma)
+        n = len(r.tokens)
+        z = self.calibrate_row(r)
+        zq, q, d = [], [], []
+        for i in range(gamma):
+            if i > 0:
+                z = M.forward_fuzzy(self.Wd, self.sd, d[-1], n + i - 1, r.draft,
+                                    self.groups, self.mode)
+            zq.append(z)
+            q.append(_dist(z, temperature))
+            d.append(draft_token(q[-1], None if greedy else draws[i], greedy))
+        r.zq, r.q, r.d = np.array(zq), np.array(q), d
+        return d
+
+    def verify_row(self, b: int, gamma: int, temperature: float, seed: int):
+        r = self.rows[b]
+        greedy = temperature == 0.0
+        draws = None if greedy else phase_draws(seed, b, r.phase, gamma)
+        n = len(r.tokens)
+        zp, p = [], []
+        for j, tok in enumerate([r.tokens[-1]] + list(r.d)):
+            z = M.forward_exact(self.Wb, self.sb, tok, n - 1 + j, r.base)
+            zp.append(z)
+            p.append(_dist(z, temperature))
+        r.zp, r.p = np.array(zp), np.array(p)
+        a, new = accept_resample(r.p, r.q, r.d,
+                                 None if greedy else draws[gamma:2 * gamma],
+                                 None if greedy else draws[2 * gamma], greedy)
+        r.n_acc = a
+        r.tokens += new
+        r.draft_len = n
+        r.phase += 1
+        return a, new
+
+    # -------------------------------------------------------------- driver
+    def generate(self, prompts, max_new: int, gamma: int, temperature: float,
+                 seed: int = 0):
+        """Speculative generation; returns [B][max_new] new tokens."""
+        self.prefill(prompts)
+        P = [len(p) for p in prompts]
+        for b, r in enumerate(self.rows):
+            while len(r.tokens) - P[b] < max_new:
+                if len(r.tokens) + gamma + 1 > self.max_len:
+                    raise ValueError("sequence would exceed max_len")
+                self.draft_row(b, gamma, temperature, seed)
+                self.verify_row(b, gamma, temperature, seed)
+        return [r.tokens[P[b]:P[b] + max_new] for b, r in enumerate(self.rows)]
+
+
+def seq_decode(Wb, shape_b: M.Shape, prompt, max_new: int, max_len: int = 256):
+    """Plain greedy decoding with the base model (the losslessness reference)."""
+    cache = M.KVCache(shape_b, max_len)
+    toks = [int(t) for t in prompt]
+    z = None
+    for pos, t in enumerate(toks):
+        z = M.forward_exact(Wb, shape_b, t, pos, cache)
+    out = []
+    for _ in range(max_new):
+        y = argmax_f32(np.asarray(z, dtype=np.float32))
+        out.append(y)
+        z = M.forward_exact(Wb, shape_b, y, len(toks), cache)
+        toks.append(y)
+    return out
+
+
+def exact_next_dist(Wb, shape_b: M.Shape, history, temperature: float, max_len: int = 256):
+    """float64 base distribution of the token following ``history`` (fresh cache)."""
+    cache = M.KVCache(shape_b, max_len)
+    z = None
+    for pos, t in enumerate(history):
+        z = M.forward_exact(Wb, shape_b, int(t), pos, cache)
+    z = np.asarray(z, dtype=np.float64) / temperature
+    e = np.exp(z - z.max())
+    return e / e.sum()

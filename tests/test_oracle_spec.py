@@ -1,0 +1,151 @@
+"""Pins for the oracle's speculative loop.
+
+What the pages fix (OpenReview discussion page, first reply, and the arXiv
+abstract page): speculative decoding is lossless, so
+  * greedy speculative output equals greedy decoding with the base alone, and
+  * sampled speculative output follows the base model's distribution;
+and calibration replaces the fuzzy draft KV entries with exact ones (reply on
+Figure 2), i.e. after calibration the draft cache equals a from-scratch
+sequential prefill of the committed tokens.
+"""
+import copy
+import multiprocessing as mp
+import os
+
+import numpy as np
+import pytest
+from scipy import stats
+
+from oracle import model as M
+from oracle import spec
+from oracle_util import tiny_pair
+
+
+def _perturbed(W, sigma, seed):
+    r = np.random.default_rng(seed)
+    out = copy.deepcopy(W)
+    for lw in out["layers"]:
+        for k, v in lw.items():
+            if v.ndim == 2:
+                v += r.normal(size=v.shape) * sigma * np.std(v)
+    return out
+
+
+CASES = [(k, mode, g) for k in (1, 2, 3) for mode in (M.ATTN_ONLY, M.FULL_LAYER) for g in (1, 4)]
+
+
+@pytest.mark.parametrize("k,mode,gamma", CASES)
+def test_greedy_speculative_equals_greedy_base(k, mode, gamma):
+    Wd, sd, Wb, sb = tiny_pair(10, std=0.3, Ld=5)
+    prompts = [[5, 6, 7, 8], [60, 1, 2]]
+    want = [spec.seq_decode(Wb, sb, p, 20, 64) for p in prompts]
+    dec = spec.SpecDecoder(Wd, sd, Wb, sb, k=k, mode=mode, max_len=64)
+    assert dec.generate(prompts, 20, gamma, 0.0) == want
+
+
+def test_greedy_selfdraft_takes_all_accepted_path():
+    # draft = base with small noise: most drafts accepted, bonus path used
+    _, _, Wb, sb = tiny_pair(11, std=0.3)
+    Wd = _perturbed(Wb, 0.02, 1)
+    dec = spec.SpecDecoder(Wd, sb, Wb, sb, k=2, mode=M.FULL_LAYER, max_len=64)
+    prompt = [3, 1, 4, 1, 5]
+    dec.prefill([prompt])
+    accepted = []
+    while len(dec.rows[0].tokens) < len(prompt) + 24:
+        dec.draft_row(0, 4, 0.0, 0)
+        a, _ = dec.verify_row(0, 4, 0.0, 0)
+        accepted.append(a)
+    assert 4 in accepted
+    assert dec.rows[0].tokens[len(prompt):len(prompt) + 24] == spec.seq_decode(Wb, sb, prompt, 24, 64)
+
+
+@pytest.mark.parametrize("mode,temp", [(M.FULL_LAYER, 0.0), (M.ATTN_ONLY, 1.0)])
+def test_calibrated_draft_cache_equals_fresh_prefill(mode, temp):
+    Wd, sd, Wb, sb = tiny_pair(12, std=0.3, Ld=5)
+    dec = spec.SpecDecoder(Wd, sd, Wb, sb, k=3, mode=mode, max_len=64)
+    dec.prefill([[9, 8, 7]])
+    r = dec.rows[0]
+    for phase in range(6):
+        dec.draft_row(0, 4, temp, 5)
+        n = r.draft_len  # calibrated prefix [0, n)
+        fresh = M.KVCache(sd, 64)
+        for pos, t in enumerate(r.tokens[:n]):
+            M.forward_exact(Wd, sd, t, pos, fresh)
+        assert np.array_equal(r.draft.K[:, :n], fresh.K[:, :n])
+        assert np.array_equal(r.draft.V[:, :n], fresh.V[:, :n])
+        if phase > 0:
+            # the previous phase wrote fuzzy entries past its committed prefix
+            assert n > 3
+        dec.verify_row(0, 4, temp, 5)
+
+
+def test_base_cache_matches_committed_tokens():
+    Wd, sd, Wb, sb = tiny_pair(13, std=0.3)
+    dec = spec.SpecDecoder(Wd, sd, Wb, sb, k=2, max_len=64)
+    dec.generate([[1, 2, 3]], 12, 3, 1.0, seed=9)
+    r = dec.rows[0]
+    n = len(r.tokens)
+    fresh = M.KVCache(sb, 64)
+    for pos, t in enumerate(r.tokens[: n - 1]):
+        M.forward_exact(Wb, sb, t, pos, fresh)
+    assert np.array_equal(r.base.K[:, : n - 1], fresh.K[:, : n - 1])
+
+
+def test_vocab_mismatch_rejected():
+    Wd, sd, Wb, sb = tiny_pair(14)
+    with pytest.raises(ValueError):
+        spec.SpecDecoder(Wd, sd._replace(vocab=65) if hasattr(sd, "_replace")
+                         else M.Shape(**{**sd.__dict__, "vocab": 65}), Wb, sb)
+
+
+# ------------------------------------------------ distribution (chi-square)
+
+_G = {}
+
+
+def _init_worker(args):
+    _G["args"] = args
+
+
+def _run_chunk(seeds):
+    Wd, sd, Wb, sb, groups, mode, prompt, gamma = _G["args"]
+    dec = spec.SpecDecoder(Wd, sd, Wb, sb, groups=groups, mode=mode, max_len=16)
+    V = sb.vocab
+    counts = np.zeros(V ** 3, np.int64)
+    for s in seeds:
+        out = dec.generate([prompt], 3, gamma, 1.0, seed=int(s))[0]
+        counts[(out[0] * V + out[1]) * V + out[2]] += 1
+    return counts
+
+
+N_DRAWS = int(os.environ.get("ES_CHISQ_DRAWS", "100000"))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("mode", [M.FULL_LAYER, M.ATTN_ONLY])
+def test_sampled_output_follows_base_distribution(mode):
+    """Joint law of the first three emitted tokens over N_DRAWS seeded runs
+    vs the brute-force base distribution (V = 8, so 512 cells).  With
+    gamma = 2 the three tokens cover the accepted, resampled and bonus
+    (all-accepted) outcomes of the first phase."""
+    Wd, sd, Wb, sb = tiny_pair(20, V=8, d=8, Ld=3, Lb=2, H=2, Hkv=1, F=8, std=0.5)
+    prompt, gamma = [1, 2, 3], 2
+    p1 = spec.exact_next_dist(Wb, sb, prompt, 1.0)
+    joint = []
+    for a in range(8):
+        p2 = spec.exact_next_dist(Wb, sb, prompt + [a], 1.0)
+        for b in range(8):
+            p3 = spec.exact_next_dist(Wb, sb, prompt + [a, b], 1.0)
+            joint.append(p1[a] * p2[b] * p3)
+    joint = np.concatenate(joint)
+    args = (Wd, sd, Wb, sb, [[0], [1, 2]], mode, prompt, gamma)
+    nproc = max(1, min(os.cpu_count() or 1, 16))
+    chunks = np.array_split(np.arange(N_DRAWS), nproc * 4)
+    with mp.get_context("spawn").Pool(nproc, initializer=_init_worker, initargs=(args,)) as pool:
+        counts = sum(pool.map(_run_chunk, chunks))
+    exp = joint * N_DRAWS
+    keep = exp >= 5
+    obs = np.append(counts[keep], counts[~keep].sum())
+    ex = np.append(exp[keep], exp[~keep].sum())
+    chi = stats.chisquare(obs, ex * obs.sum() / ex.sum())
+    assert chi.pvalue > 1e-3, (chi, counts, exp)
