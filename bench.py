@@ -1,0 +1,386 @@
+#!/usr/bin/env python
+"""Benchmark: EasySpec layer-parallel speculative decoding on one B300.
+
+One step = one speculative generation of `max_new` tokens at batch 1 for the
+workload (default: Qwen2.5-shaped bf16 pair, 0.5B-shaped draft / 7B-shaped
+base, 256-token prompt, gamma 4, 128 new tokens, layer-set size k = 4,
+temperature 1.0), random-initialised weights and uniform prompt ids.
+
+  value      decode tokens/s with the prompt already prefilled in HBM: CUDA
+             events on the library's stream around es_decode (all phases:
+             calibration + fuzzy drafts + verification + accept/resample)
+  e2e        the same generation through the C-ABI call generate() with host
+             buffers: prompt upload, both prefills, decoding and the token
+             read-back inside the timed region (host wall clock)
+  draft/verify  per-phase breakdown (CUDA events around draft_step and
+             verify_step) and their fraction of the HBM weight-stream
+             roofline: bytes = weights streamed + KV read/written
+  roofline   the dominant kernel (most device time in a per-launch event
+             pass over one generation): algorithmic bytes / event time vs the
+             measured HBM copy bandwidth
+  cpu_baseline  the CPU oracle (float64 numpy) on a bounded sample
+
+With --impl reference the oracle arm runs instead (CPU only).
+Multi-GPU (torchrun): independent replicas, one per GPU; no collective on
+the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "qwen2.5_0.5b_7b_bf16"
+METRIC = "draft & end-to-end tok/s, bs=1, 1xB300; % of HBM weight-stream roofline"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--k", type=int, default=4)
+    ap.add_argument("--mode", default="full", choices=["full", "attn"])
+    ap.add_argument("--temperature", type=float, default=1.0)
+    ap.add_argument("--gamma", type=int, default=None)
+    ap.add_argument("--breakdown-phases", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ bytes model
+def weight_bytes(s: dict, esz: int) -> dict:
+    d, hd, F, V = s["d"], s["head_dim"], s["ffn"], s["vocab"]
+    qd, kvd = s["n_heads"] * hd, s["n_kv_heads"] * hd
+    layer = (qd * d + 2 * kvd * d + d * qd + 3 * F * d + 2 * d) * esz
+    return {"layers": s["n_layers"] * layer, "head": (V * d + d) * esz, "embed_row": d * esz}
+
+
+def kv_bytes(s: dict, esz: int, ctx: int, rows: int) -> float:
+    """K/V read by `rows` queries at context ~ctx plus the rows' K/V writes."""
+    per_pos = 2 * s["n_kv_heads"] * s["head_dim"] * esz * s["n_layers"]
+    return per_pos * (ctx * rows + rows)
+
+
+def phase_bytes(wl: dict, gamma: int, ctx: int) -> dict:
+    esz = 2 if wl["dtype"] == "bf16" else 4
+    wd, wb = weight_bytes(wl["draft"], esz), weight_bytes(wl["base"], esz)
+    draft_fwd = wd["layers"] + wd["head"] + wd["embed_row"]
+    draft = gamma * draft_fwd + kv_bytes(wl["draft"], esz, ctx, 2 * gamma)
+    verify = wb["layers"] + wb["head"] + (gamma + 1) * wb["embed_row"] + kv_bytes(wl["base"], esz, ctx, gamma + 1)
+    return {"draft_fwd": draft_fwd, "draft": draft, "verify": verify}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6400.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={gpu_id}", f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.p = None
+
+    def stop(self) -> dict:
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        self.p.wait()
+        self.f.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.f.read().splitlines():
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.f.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample(wl: dict, gamma: int, tokens_per_phase: float, reps: int = 2, seed: int = 0):
+    """Time the CPU oracle on a bounded sample of the workload: one exact
+    decoder layer and the output head of each model at full width (2-layer
+    truncated models, float64 numpy, context ~prompt+64 filled with random
+    K/V), scaled to the full depth and to one speculative phase
+    (calibration of tokens_per_phase tokens + gamma-1 fuzzy forwards +
+    gamma+1 verified tokens, one token at a time as the oracle runs)."""
+    import torch
+
+    from layer_drafting_draft_b300 import synth
+    from oracle import model as M
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    ctx = wl["prompt"] + 64
+    per = {}
+    for which in ("draft", "base"):
+        s = dict(wl[which], n_layers=2)
+        W = M.as_f64_weights(synth.make_weights(s, 7 + seed, wl["dtype"], dev))
+        shape = M.Shape(**s)
+        cache = M.KVCache(shape, ctx + 8)
+        r = np.random.default_rng(1)
+        cache.K[:, :ctx] = r.normal(size=cache.K[:, :ctx].shape)
+        cache.V[:, :ctx] = r.normal(size=cache.V[:, :ctx].shape)
+        h = W["embed"][3].copy()
+        t0 = time.perf_counter()
+        for i in range(reps):
+            for l in range(2):
+                h = M.layer_exact(W, shape, l, h, ctx + i, cache)
+        t_layer = (time.perf_counter() - t0) / (2 * reps)
+        t0 = time.perf_counter()
+        for i in range(reps):
+            M.head_logits(W, shape, h)
+        t_head = (time.perf_counter() - t0) / reps
+        per[which] = wl[which]["n_layers"] * t_layer + t_head
+        del W, cache
+    phase_s = (tokens_per_phase + gamma - 1) * per["draft"] + (gamma + 1) * per["base"]
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+    except Exception:
+        cores = os.cpu_count()
+    return {"value": tokens_per_phase / phase_s, "unit": "tok/s", "cores": cores, "kind": "oracle",
+            "sample": (f"float64 numpy oracle: one exact layer + output head of each model at full "
+                       f"width (2-layer truncations), {reps} tokens each, context {ctx}; per-token "
+                       f"cost scaled to {wl['draft']['n_layers']}+{wl['base']['n_layers']} layers and "
+                       f"to one phase of {tokens_per_phase:.2f} committed tokens (gamma {gamma})"),
+            "draft_forward_s": per["draft"], "base_token_s": per["base"]}
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args, rank: int, world: int):
+    import torch
+
+    from layer_drafting_draft_b300 import build, synth
+    from layer_drafting_draft_b300.easyspec import ES_ATTN_ONLY, ES_FULL_LAYER, EasySpec
+    build.build()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    wl = synth.WORKLOADS[args.workload]
+    gamma = args.gamma or wl["gamma"]
+    P, max_new, T, k = wl["prompt"], wl["max_new"], args.temperature, args.k
+    draft_w, base_w, prompts = synth.make_pair(args.workload, device="cuda")
+    prompts = prompts[:1].numpy() if wl["batch"] >= 1 else prompts.numpy()
+    stream = torch.cuda.Stream()
+    mode = ES_FULL_LAYER if args.mode == "full" else ES_ATTN_ONLY
+    max_seq = ((P + max_new + 2 * gamma + 2) + 63) // 64 * 64
+    g = EasySpec(draft_w, wl["draft"], base_w, wl["base"], wl["dtype"], 1, max_seq, gamma, mode,
+                 None, stream)
+    seed0 = 1000 * rank
+
+    def one_decode(step):
+        g.easyspec_prefill(prompts)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        st = g.es_decode(max_new, gamma, k, T, seed0 + step)
+        ev1.record(stream)
+        ev1.synchronize()
+        return ev0.elapsed_time(ev1), st
+
+    for w in range(args.warmup):
+        one_decode(10_000 + w)
+    barrier(world)
+    torch.cuda.synchronize()
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    uuid = getattr(props, "uuid", None)
+    clocks = Clocks(f"GPU-{uuid}" if uuid is not None else str(torch.cuda.current_device()))
+    dec_ms, stats = [], []
+    t_wall = time.perf_counter()
+    for s in range(args.steps):
+        ms, st = one_decode(s)
+        dec_ms.append(ms)
+        stats.append(st)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    barrier(world)
+    total_ms = max_over_ranks(sum(dec_ms), world)
+    value = world * args.steps * max_new / (total_ms / 1e3)
+    emitted = sum(s["emitted"] for s in stats)
+    phases = sum(s["phases"] for s in stats)
+    accepted = sum(s["accepted"] for s in stats)
+    drafted = sum(s["drafted"] for s in stats)
+    launches = sum(s["kernel_launches"] for s in stats)
+    tok_per_phase = emitted / max(phases, 1)
+
+    # ---- per-phase breakdown (draft part / verify part), CUDA events
+    g.easyspec_prefill(prompts)
+    d_ms, v_ms = [], []
+    for i in range(args.breakdown_phases):
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        g.draft_step(k, gamma, T, 77 + i)
+        e1.record(stream)
+        g.verify_step(T, 77 + i, gamma)
+        e2.record(stream)
+        e2.synchronize()
+        if i > 0:
+            d_ms.append(e0.elapsed_time(e1))
+            v_ms.append(e1.elapsed_time(e2))
+    peak, peak_src = peaks()
+    pb = phase_bytes(wl, gamma, P + max_new // 2)
+    draft_ms, verify_ms = statistics.median(d_ms), statistics.median(v_ms)
+    draft_gbs = pb["draft"] / (draft_ms * 1e-3) / 1e9
+    verify_gbs = pb["verify"] / (verify_ms * 1e-3) / 1e9
+    phase_roof_s = (pb["draft"] + pb["verify"]) / (peak * 1e9)
+    roof_tok_s = tok_per_phase / phase_roof_s
+
+    # ---- e2e through generate() with host buffers
+    e2e_ms = []
+    out_host = None
+    for s in range(max(2, args.steps)):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        out_host, _ = g.generate(prompts, max_new, gamma, k, T, seed0 + 500 + s)
+        e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    e2e_value = world * max_new / (max_over_ranks(statistics.mean(e2e_ms), world) / 1e3)
+
+    # ---- dominant kernel: per-launch event pass over one generation
+    g.easyspec_prefill(prompts)
+    g.es_profile(True)
+    g.es_decode(max_new, gamma, k, T, seed0 + 999)
+    prof = g.es_profile_read()
+    g.es_profile(False)
+    top = max((kv for kv in prof.items() if kv[1][2] > 0), key=lambda kv: kv[1][0])
+    name, (pms, pn, pbytes) = top
+    achieved = pbytes / (pms * 1e-3) / 1e9
+    total_prof_ms = sum(v[0] for v in prof.values())
+    g.close()
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl["dtype"], "data": "synthetic",
+        "config": {"workload": args.workload, "draft": "24L d896 14H/2KV ffn4864 V151936",
+                   "base": "28L d3584 28H/4KV ffn18944 V151936", "batch": 1, "prompt": P,
+                   "max_new": max_new, "gamma": gamma, "k": k, "mode": args.mode,
+                   "temperature": T, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (weights 16.5 GB streamed per phase)"},
+        "e2e": {"value": round(e2e_value, 2), "unit": "tok/s",
+                "h2d_bytes_per_step": int(prompts.size * 4 + 16 + 8),
+                "d2h_bytes_per_step": int(max_new * 4)},
+        "draft": {"tok_s": round(gamma / (draft_ms * 1e-3), 1), "ms_per_phase": round(draft_ms, 4),
+                  "achieved_gbs": round(draft_gbs, 1), "roofline_frac": round(draft_gbs / peak, 4),
+                  "bytes_per_phase": int(pb["draft"])},
+        "verify": {"ms_per_phase": round(verify_ms, 4), "achieved_gbs": round(verify_gbs, 1),
+                   "roofline_frac": round(verify_gbs / peak, 4), "bytes_per_phase": int(pb["verify"])},
+        "weight_stream_roofline": {"tok_s": round(roof_tok_s, 1), "e2e_frac": round(value / world / roof_tok_s, 4),
+                                   "peak_gbs": peak, "peak_source": peak_src},
+        "acceptance": {"tokens_per_phase": round(tok_per_phase, 3),
+                       "rate": round(accepted / max(drafted, 1), 4)},
+        "roofline": {"bound": "hbm", "kernel": name, "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "launches": pn, "share_of_device_time": round(pms / total_prof_ms, 4),
+                     "peak_source": peak_src},
+        "clocks": clk, "gpu_launches": int(launches),
+        "timed_wall_s": round(wall, 3),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_sample(wl, gamma, tok_per_phase)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args, rank: int, world: int):
+    """The oracle arm: the CPU oracle timed on this host's cores."""
+    if rank != 0:
+        return
+    from layer_drafting_draft_b300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    gamma = args.gamma or wl["gamma"]
+    # committed tokens per phase: the run's own acceptance is unknown on the
+    # CPU arm; one token per phase (no acceptance) is the conservative sample
+    for w in range(args.warmup):
+        oracle_sample(wl, gamma, 1.0, reps=1, seed=w)
+    vals = []
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        vals.append(oracle_sample(wl, gamma, 1.0, reps=1, seed=100 + s))
+    wall = time.perf_counter() - t0
+    v = statistics.mean(x["value"] for x in vals)
+    cb = dict(vals[-1])
+    cb["value"] = v
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload, "gamma": gamma, "batch": 1},
+            "cpu_baseline": cb, "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0,
+                                        "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ distributed
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    args = parse()
+    rank, world = dist_env()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if (torch.cuda.is_available() and args.impl == "ours") else "gloo")
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

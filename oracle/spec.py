@@ -98,24 +98,31 @@ class SpecDecoder:
         r.draft_len = len(r.tokens)
         return z
 
-    def draft_row(self, b: int, gamma: int, temperature: float, seed: int):
+    def draft_row(self, b: int, gamma: int, temperature: float, seed: int, force_d=None):
+        """Calibration + gamma-1 fuzzy forwards.  ``force_d`` (checking aid)
+        replaces the drawn tokens by given ones; the oracle's own draws are
+        kept in ``row.d_own``."""
         r = self.rows[b]
         greedy = temperature == 0.0
         draws = None if greedy else phase_draws(seed, b, r.phase, gamma)
         n = len(r.tokens)
         z = self.calibrate_row(r)
-        zq, q, d = [], [], []
+        zq, q, d, own = [], [], [], []
         for i in range(gamma):
             if i > 0:
                 z = M.forward_fuzzy(self.Wd, self.sd, d[-1], n + i - 1, r.draft,
                                     self.groups, self.mode)
             zq.append(z)
             q.append(_dist(z, temperature))
-            d.append(draft_token(q[-1], None if greedy else draws[i], greedy))
-        r.zq, r.q, r.d = np.array(zq), np.array(q), d
+            own.append(draft_token(q[-1], None if greedy else draws[i], greedy))
+            d.append(own[-1] if force_d is None else int(force_d[i]))
+        r.zq, r.q, r.d, r.d_own = np.array(zq), np.array(q), d, own
         return d
 
-    def verify_row(self, b: int, gamma: int, temperature: float, seed: int):
+    def verify_row(self, b: int, gamma: int, temperature: float, seed: int, force=None):
+        """Verification + accept/resample + commit.  ``force`` = (a, tokens)
+        (checking aid) commits given decisions; the oracle's own are kept in
+        ``row.own``."""
         r = self.rows[b]
         greedy = temperature == 0.0
         draws = None if greedy else phase_draws(seed, b, r.phase, gamma)
@@ -129,6 +136,9 @@ class SpecDecoder:
         a, new = accept_resample(r.p, r.q, r.d,
                                  None if greedy else draws[gamma:2 * gamma],
                                  None if greedy else draws[2 * gamma], greedy)
+        r.own = (a, new)
+        if force is not None:
+            a, new = int(force[0]), [int(t) for t in force[1]]
         r.n_acc = a
         r.tokens += new
         r.draft_len = n
