@@ -30,8 +30,9 @@
  *     default stream).  Calls that return host results synchronise that
  *     stream before returning; the others are asynchronous.
  *   - Matrices are row-major [out_features, in_features].  Every in_features
- *     (d, ffn, n_heads*head_dim) must be a multiple of 8, head_dim must be
- *     even and <= 256, and n_heads a multiple of n_kv_heads (ES_ERR_ARG).
+ *     (d, ffn, n_heads*head_dim) must be a multiple of 8, head_dim a multiple
+ *     of 8 and <= 256, and n_heads a multiple of n_kv_heads with at most 16
+ *     query heads per kv head (ES_ERR_ARG).
  */
 #ifndef EASYSPEC_H_
 #define EASYSPEC_H_

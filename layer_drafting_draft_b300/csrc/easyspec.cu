@@ -6,6 +6,7 @@
 #include <chrono>
 #include <cmath>
 #include <cstdarg>
+#include <cstddef>
 #include <cstdio>
 #include <cstring>
 #include <map>
@@ -41,32 +42,21 @@ struct ArgError { std::string msg; es_status st; };
 
 struct Layer { const void *an, *wq, *wk, *wv, *wo, *mn, *wg, *wu, *wd; };
 
-struct GemvLaunch {
-    const GemvOp* ops = nullptr;
-    int nops = 0, gemv_tiles = 0, gemm_tiles = 0;
-    // algorithmic bytes of one launch over M rows: wbytes + M * rowbytes
-    // (weights once; per input row its activations read and outputs written)
-    double wbytes = 0, rowbytes = 0;
-    double bytes(int M) const { return wbytes + (double)M * rowbytes; }
+// One kernel launch of a planned forward pass.
+enum RecKind { R_GV = 0, R_GEMM = 1, R_NORM = 2, R_ATTN = 3 };
+struct Rec {
+    int kind = R_GV;
+    const char* name = "";
+    double bytes = 0;          // algorithmic bytes (weights + activations), 0 if not modelled
+    const GvLaunch* gv = nullptr;
+    int grid = 0, smem = 0, M = 0, ntiles64 = 0;
+    NormArgs norm{};
+    AttnArgs attn{};
+    dim3 g3;
 };
 
 struct ProfRec { const char* name; double bytes; cudaEvent_t a, b; };
 struct ProfAgg { double ms = 0, bytes = 0; int64_t launches = 0; };
-
-// One layer set of a forward plan.
-struct GroupPlan {
-    int first = 0, n = 1;
-    bool fuzzy = false;
-    NormArgs norm_in{};
-    GemvLaunch wide;
-    RopeArgs rope{};
-    AttnArgs attn{};
-    GemvLaunch o;                      // exact: o (acc into h); ATTN_ONLY set: A_j (store)
-    int n_mlp = 0;                     // sequential MLPs (exact: 1, ATTN_ONLY set: n)
-    NormArgs norm_mlp[MAX_GROUP]{};
-    GemvLaunch swi[MAX_GROUP], down[MAX_GROUP];
-    GemvLaunch kcat;                   // FULL_LAYER set: o (+) down, acc into h
-};
 
 struct Model {
     int L = 0, d = 0, H = 0, Hkv = 0, hd = 0, F = 0, V = 0, qd = 0, kvd = 0, dtype = 0;
@@ -79,8 +69,7 @@ struct Model {
     int slots = 1, Mw = 0, nsplit = 0;
     float *h = nullptr, *xf = nullptr, *part = nullptr;
     std::vector<float*> xb, mb, q, k, v, a, s, A;
-    int *row_pos = nullptr, *row_seq = nullptr, *row_tok = nullptr;
-    NormArgs head_norm{};
+    int *row_pos = nullptr, *row_seq = nullptr, *row_tok = nullptr, *row_base = nullptr;
 };
 
 struct Graph { cudaGraphExec_t exec = nullptr; int64_t kernels = 0; };
@@ -108,13 +97,21 @@ struct es_ctx {
     float *q_logits = nullptr, *q_probs = nullptr, *p_logits = nullptr, *p_probs = nullptr;
     RunParams* prm = nullptr;
     int* status = nullptr;
+    // scratch of the split kernels (partials and arrival counters)
+    float* gv_scratch = nullptr;
+    int* gv_counters = nullptr;
+    int* att_counters = nullptr;
+    float* sm_part = nullptr;
+    unsigned long long* sm_mass = nullptr;
+    int* sm_counters = nullptr;
+    int sm_rows_cap = 0, sm_nb_cap = 0;
     // pinned host mirrors
     RunParams* h_prm = nullptr;
     int* h_small = nullptr;  // n_acc | out_tok | n_commit | status
 
-    GemvOp* arena = nullptr;
-    int arena_cap = 0, arena_used = 0;
-    size_t cur_esz = 2;  // weight element size of the model being planned
+    // launch descriptors (GEMV launches) live in a device arena
+    char* arena = nullptr;
+    size_t arena_cap = 0, arena_used = 0;
 
     // session state
     int B = 0;
@@ -132,8 +129,10 @@ struct es_ctx {
     size_t prof_pool_used = 0;
     std::map<std::string, ProfAgg> prof;
 
-    std::map<int, std::vector<GroupPlan>> plans;  // key: k (0 = explicit sets)
-    std::map<std::tuple<int, int, int>, GemvLaunch> heads;  // (gamma, kind, step)
+    // planned forwards: key (model 0 draft / 1 base, set key, rows)
+    std::map<std::tuple<int, int, int>, std::vector<Rec>> plans;
+    // planned output heads: key (model, rows, row stride, row offset, y, ldy)
+    std::map<std::tuple<int, int, int, int, const float*, int>, std::vector<Rec>> heads;
     std::map<std::tuple<int, int, int, int>, Graph> graphs;  // (part, gamma, k, B)
 
     template <typename T>
@@ -153,7 +152,7 @@ namespace {
 // ------------------------------------------------------------------ launch helper
 template <typename... KArgs, typename... Args>
 void launch(es_ctx* c, const char* name, double bytes, void (*kern)(KArgs...), dim3 grid,
-            dim3 block, Args... args) {
+            dim3 block, size_t smem, Args... args) {
     if (grid.x == 0 || grid.y == 0 || grid.z == 0) return;
     cudaEvent_t ev0 = nullptr, ev1 = nullptr;
     if (c->profiling) {
@@ -171,7 +170,7 @@ void launch(es_ctx* c, const char* name, double bytes, void (*kern)(KArgs...), d
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = c->st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -202,13 +201,13 @@ void prof_collect(es_ctx* c) {
 
 // ------------------------------------------------------------------ model setup
 void check_shape(const es_model_shape& s, const char* which) {
-    if (s.n_layers < 1 || s.d < 8 || s.n_heads < 1 || s.n_kv_heads < 1 || s.head_dim < 2 ||
+    if (s.n_layers < 1 || s.d < 8 || s.n_heads < 1 || s.n_kv_heads < 1 || s.head_dim < 8 ||
         s.ffn < 8 || s.vocab < 2)
         arg_fail(ES_ERR_ARG, "%s: non-positive shape field", which);
     if (s.d % 8 || s.ffn % 8 || (s.n_heads * s.head_dim) % 8)
         arg_fail(ES_ERR_ARG, "%s: d, ffn and n_heads*head_dim must be multiples of 8", which);
-    if (s.head_dim % 2 || s.head_dim > 256)
-        arg_fail(ES_ERR_ARG, "%s: head_dim must be even and <= 256", which);
+    if (s.head_dim % 8 || s.head_dim > 256)
+        arg_fail(ES_ERR_ARG, "%s: head_dim must be a multiple of 8 and <= 256", which);
     if (s.n_heads % s.n_kv_heads || s.n_heads / s.n_kv_heads > MAX_GQA)
         arg_fail(ES_ERR_ARG, "%s: n_heads must be a multiple of n_kv_heads (ratio <= %d)", which, MAX_GQA);
     if (s.dtype != ES_DTYPE_F32 && s.dtype != ES_DTYPE_BF16)
@@ -285,43 +284,89 @@ void setup_model(es_ctx* c, Model& m, const es_model_shape& s, const es_weights*
     m.row_pos = c->dalloc<int>(Mw);
     m.row_seq = c->dalloc<int>(Mw);
     m.row_tok = c->dalloc<int>(Mw);
+    m.row_base = c->dalloc<int>(Mw);
 }
 
-// ------------------------------------------------------------------ op descriptors
-GemvLaunch upload_ops(es_ctx* c, std::vector<GemvOp> ops) {
-    GemvLaunch gl;
-    int t8 = 0, t64 = 0;
-    for (auto& op : ops) { op.tile0 = t8; t8 += (op.N + GEMV_WARPS - 1) / GEMV_WARPS; }
-    // gemm tiles are derived from the same ops with a 64-row tile: store a
-    // second copy with tile0 in 64-row units right after the first
-    std::vector<GemvOp> ops64 = ops;
-    for (auto& op : ops64) { op.tile0 = t64; t64 += (op.N + GB - 1) / GB; }
-    const int n = (int)ops.size();
-    if (c->arena_used + 2 * n > c->arena_cap) arg_fail(ES_ERR_OOM, "op descriptor arena exhausted");
-    GemvOp* dst = c->arena + c->arena_used;
-    CK(cudaMemcpy(dst, ops.data(), n * sizeof(GemvOp), cudaMemcpyHostToDevice));
-    CK(cudaMemcpy(dst + n, ops64.data(), n * sizeof(GemvOp), cudaMemcpyHostToDevice));
-    c->arena_used += 2 * n;
-    gl.ops = dst; gl.nops = n; gl.gemv_tiles = t8; gl.gemm_tiles = t64;
-    for (const auto& op : ops) {
-        for (int s = 0; s < op.nseg; ++s) {
-            gl.wbytes += (double)op.N * op.seg[s].K * c->cur_esz;
-            gl.rowbytes += (double)op.seg[s].K * 4.0;
-        }
-        gl.rowbytes += (double)op.N * 4.0 * (op.epi == EPI_ACC ? 2 : 1);
+// ------------------------------------------------------------------ GEMV launch building
+// Collects the ops and activation sources of one weight-streaming launch.
+struct GvBuild {
+    GvLaunch L;
+    size_t esz;
+    int xfloats = 0;
+    bool simt;  // many-row launch (SIMT GEMM): every source read from global memory
+    GvBuild(int M, float eps, size_t esz_, bool simt_) : esz(esz_), simt(simt_) {
+        memset(&L, 0, sizeof L);
+        L.M = M;
+        L.eps = eps;
     }
-    return gl;
-}
+    // Register an activation source; -1 when a normalised source does not
+    // fit in shared memory (the caller then normalises it beforehand).
+    int source(const float* src, const float* add, const void* gain, int K, int ld, int rs, int ro,
+               int kind) {
+        if (L.nxs >= GV_MAX_XS) arg_fail(ES_ERR_ARG, "too many activation sources in one launch");
+        const int need = L.M * K;
+        int off = -1;
+        if (!simt && xfloats + need <= GV_XSMEM_MAX) { off = xfloats; xfloats += (need + 3) & ~3; }
+        if (kind == XS_NORM && off < 0) return -1;
+        GvXSrc& x = L.xs[L.nxs];
+        x.src = src; x.add = add; x.gain = gain; x.K = K; x.ld = ld; x.row_stride = rs; x.row_off = ro;
+        x.kind = kind; x.smem_off = off;
+        return L.nxs++;
+    }
+    GvOp& op(int N, float* y, int ldy, int epi, const float* add = nullptr) {
+        if (L.nops >= GV_MAX_OPS) arg_fail(ES_ERR_ARG, "too many ops in one launch");
+        GvOp& o = L.ops[L.nops++];
+        o.N = N; o.y = y; o.ldy = ldy; o.epi = epi; o.add = add;
+        return o;
+    }
+    void seg(GvOp& o, const void* W, int K, int xs, int set) {
+        if (o.nseg >= GV_MAX_SEG) arg_fail(ES_ERR_ARG, "too many K-concatenated segments");
+        if (xs < 0 || L.xs[xs].K != K) arg_fail(ES_ERR_ARG, "segment / source width mismatch");
+        GvSeg& s = o.seg[o.nseg++];
+        s.W = W; s.K = K; s.xs = xs; s.set = set;
+    }
+};
 
-GemvOp make_op(int N, float* y, int ldy, int epi) {
-    GemvOp op;
-    memset(&op, 0, sizeof op);
-    op.N = N; op.y = y; op.ldy = ldy; op.epi = epi;
-    return op;
-}
-void add_seg(GemvOp& op, const void* W, const float* x, int K, int ldx) {
-    if (op.nseg >= MAX_SEG) arg_fail(ES_ERR_ARG, "too many K-concatenated segments");
-    op.seg[op.nseg++] = GemvSeg{W, x, K, ldx};
+Rec finish_gv(es_ctx* c, GvBuild& b, const char* name) {
+    GvLaunch& L = b.L;
+    const int SC = GV_ROW_BYTES / (int)b.esz;
+    int t = 0, st = 0, t64 = 0;
+    double wbytes = 0, rowbytes = 0;
+    for (int i = 0; i < L.nops; ++i) {
+        GvOp& o = L.ops[i];
+        o.spt = 0;
+        for (int s = 0; s < o.nseg; ++s) {
+            o.seg[s].nck = (o.seg[s].K + SC - 1) / SC;
+            o.spt += o.seg[s].nck;
+            wbytes += (double)o.N * o.seg[s].K * b.esz;
+        }
+        o.ntiles = (o.N + GV_RT - 1) / GV_RT;
+        o.tile0 = t; o.stage0 = st; o.tile64_0 = t64;
+        t += o.ntiles; st += o.ntiles * o.spt; t64 += (o.N + GB - 1) / GB;
+        rowbytes += (double)o.N * 4.0 * (o.epi == GEPI_STORE || o.epi == GEPI_SWIGLU ? 1 : o.epi == GEPI_ACC ? 2 : 3);
+    }
+    for (int i = 0; i < L.nxs; ++i) rowbytes += (double)L.xs[i].K * 4.0 * (L.xs[i].add ? 2 : 1);
+    L.ntiles = t; L.nstages = st; L.ntiles64 = t64;
+    const int ctas = c->num_sms * GV_CTAS_PER_SM;
+    L.q = std::max(1, (st + ctas - 1) / ctas);
+    L.x_smem_floats = b.xfloats;
+    if (t > GV_COUNTERS) arg_fail(ES_ERR_ARG, "launch has %d tiles (> %d)", t, GV_COUNTERS);
+    Rec r;
+    r.kind = b.simt ? R_GEMM : R_GV;
+    r.name = name;
+    r.M = L.M;
+    r.grid = (st + L.q - 1) / L.q;
+    r.smem = b.xfloats * (int)sizeof(float);
+    r.ntiles64 = t64;
+    r.bytes = wbytes + L.M * rowbytes;
+    // upload the used prefix of the descriptor
+    const size_t bytes = offsetof(GvLaunch, ops) + (size_t)L.nops * sizeof(GvOp);
+    const size_t at = (c->arena_used + 255) & ~(size_t)255;
+    if (at + bytes > c->arena_cap) arg_fail(ES_ERR_OOM, "launch descriptor arena exhausted");
+    CK(cudaMemcpy(c->arena + at, &L, bytes, cudaMemcpyHostToDevice));
+    c->arena_used = at + bytes;
+    r.gv = reinterpret_cast<const GvLaunch*>(c->arena + at);
+    return r;
 }
 
 NormArgs norm_args(Model& m, float* h, const float* add) {
@@ -336,98 +381,153 @@ void add_job(NormArgs& a, const void* g, float* out) {
     a.out[a.njobs] = out;
     a.njobs++;
 }
-
-RopeArgs rope_args(Model& m) {
-    RopeArgs r;
-    memset(&r, 0, sizeof r);
-    r.g = m.g; r.rope = m.rope; r.H = m.H; r.row_pos = m.row_pos; r.row_seq = m.row_seq;
+Rec norm_rec(const NormArgs& a, int rows) {
+    Rec r;
+    r.kind = R_NORM; r.name = "rmsnorm"; r.norm = a; r.M = rows;
     return r;
 }
-AttnArgs attn_args(Model& m) {
-    AttnArgs a;
+
+Rec attn_rec(es_ctx* c, Model& m, int l0, int n, int M) {
+    if ((size_t)M * n * m.Hkv > (size_t)ATT_COUNTERS) arg_fail(ES_ERR_ARG, "attention launch too large");
+    Rec r;
+    r.kind = R_ATTN; r.name = "attention";
+    AttnArgs& a = r.attn;
     memset(&a, 0, sizeof a);
-    a.g = m.g; a.H = m.H; a.nsplit = m.nsplit; a.part = m.part; a.row_pos = m.row_pos;
-    a.row_seq = m.row_seq;
-    return a;
+    a.g = m.g; a.rope = m.rope; a.H = m.H; a.M = M; a.nl = n; a.nsplit = m.nsplit;
+    for (int j = 0; j < n; ++j) {
+        a.layer[j] = l0 + j;
+        a.q[j] = m.q[j]; a.k[j] = m.k[j]; a.v[j] = m.v[j]; a.out[j] = m.a[j];
+    }
+    a.part = m.part; a.counters = c->att_counters;
+    a.row_pos = m.row_pos; a.row_seq = m.row_seq; a.row_base = m.row_base;
+    r.g3 = dim3(M, n * m.Hkv, m.nsplit);
+    r.smem = (int)attn_smem_bytes(m.H / m.Hkv, m.hd);
+    r.M = M;
+    return r;
 }
 
-// Plan of one forward pass for the layer sets `groups` (sets of one layer are
-// exact layers).
-std::vector<GroupPlan> build_plan(es_ctx* c, Model& m, const std::vector<std::vector<int>>& groups,
-                                  int mode) {
-    std::vector<GroupPlan> plan;
+// Plan of one forward pass over M rows for the layer sets `groups` (sets of
+// one layer are exact layers).  M <= GV_MAXM: fused weight-streaming launches
+// (norms inside the GEMV, RoPE and KV append inside attention); larger M:
+// explicit norm launches and the SIMT GEMM.
+std::vector<Rec> build_forward(es_ctx* c, Model& m, const std::vector<std::vector<int>>& groups,
+                               int mode, int M) {
+    const bool fast = M <= GV_MAXM;
+    std::vector<Rec> out;
+    // an activation RMSNorm(h [+ add]) * gain: fused when it fits, else a
+    // norm launch (which also folds `add` into h) writes it to `buf`;
+    // returns the source index and whether it was fused
+    auto norm_source = [&](GvBuild& b, NormArgs& pre, const void* gain, float* buf,
+                           const float* add, bool* fused) -> int {
+        if (fast) {
+            const int xs = b.source(m.h, add, gain, m.d, m.d, 1, 0, XS_NORM);
+            if (xs >= 0) { if (fused) *fused = true; return xs; }
+        }
+        if (fused) *fused = false;
+        if (pre.add != add && pre.njobs) arg_fail(ES_ERR_ARG, "internal: mixed norm inputs");
+        pre.add = add;
+        add_job(pre, gain, buf);
+        return b.source(buf, nullptr, nullptr, m.d, m.d, 1, 0, XS_RAW);
+    };
+    auto raw = [&](GvBuild& b, const float* p, int K) {
+        return b.source(p, nullptr, nullptr, K, K, 1, 0, XS_RAW);
+    };
     for (const auto& gl : groups) {
-        GroupPlan gp;
-        gp.first = gl.front();
-        gp.n = (int)gl.size();
-        gp.fuzzy = gp.n > 1;
-        if (gp.n > m.slots || gp.n > MAX_GROUP) arg_fail(ES_ERR_ARG, "layer set larger than %d", MAX_GROUP);
-        const int n = gp.n;
-        const bool full = gp.fuzzy && mode == ES_FULL_LAYER;
-        // input norms from the set input h
-        gp.norm_in = norm_args(m, m.h, nullptr);
-        for (int j = 0; j < n; ++j) add_job(gp.norm_in, m.ly[gp.first + j].an, m.xb[j]);
-        if (full)
-            for (int j = 0; j < n; ++j) add_job(gp.norm_in, m.ly[gp.first + j].mn, m.mb[j]);
-        // wide pass: q,k,v of every layer (+ SwiGLU of every layer for FULL_LAYER)
-        std::vector<GemvOp> wide;
-        for (int j = 0; j < n; ++j) {
-            const Layer& y = m.ly[gp.first + j];
-            GemvOp oq = make_op(m.qd, m.q[j], m.qd, EPI_STORE); add_seg(oq, y.wq, m.xb[j], m.d, m.d);
-            GemvOp ok = make_op(m.kvd, m.k[j], m.kvd, EPI_STORE); add_seg(ok, y.wk, m.xb[j], m.d, m.d);
-            GemvOp ov = make_op(m.kvd, m.v[j], m.kvd, EPI_STORE); add_seg(ov, y.wv, m.xb[j], m.d, m.d);
-            wide.push_back(oq); wide.push_back(ok); wide.push_back(ov);
-        }
-        if (full)
+        const int n = (int)gl.size(), l0 = gl.front();
+        if (n > m.slots || n > MAX_GROUP) arg_fail(ES_ERR_ARG, "layer set larger than %d", MAX_GROUP);
+        const bool fuzzy = n > 1, full = fuzzy && mode == ES_FULL_LAYER;
+        // ---- wide pass: q, k, v of every layer (+ SwiGLU of every layer)
+        {
+            GvBuild b(M, m.eps, m.esz, !fast);
+            NormArgs pre = norm_args(m, m.h, nullptr);
+            int xa[MAX_GROUP], xm[MAX_GROUP];
+            for (int j = 0; j < n; ++j) xa[j] = norm_source(b, pre, m.ly[l0 + j].an, m.xb[j], nullptr, nullptr);
+            if (full)
+                for (int j = 0; j < n; ++j) xm[j] = norm_source(b, pre, m.ly[l0 + j].mn, m.mb[j], nullptr, nullptr);
             for (int j = 0; j < n; ++j) {
-                const Layer& y = m.ly[gp.first + j];
-                GemvOp os = make_op(m.F, m.s[j], m.F, EPI_SWIGLU);
-                add_seg(os, y.wg, m.mb[j], m.d, m.d);
-                add_seg(os, y.wu, m.mb[j], m.d, m.d);
-                wide.push_back(os);
+                const Layer& y = m.ly[l0 + j];
+                b.seg(b.op(m.qd, m.q[j], m.qd, GEPI_STORE), y.wq, m.d, xa[j], 0);
+                b.seg(b.op(m.kvd, m.k[j], m.kvd, GEPI_STORE), y.wk, m.d, xa[j], 0);
+                b.seg(b.op(m.kvd, m.v[j], m.kvd, GEPI_STORE), y.wv, m.d, xa[j], 0);
             }
-        gp.wide = upload_ops(c, wide);
-        gp.rope = rope_args(m);
-        gp.attn = attn_args(m);
-        gp.rope.nl = gp.attn.nl = n;
-        for (int j = 0; j < n; ++j) {
-            gp.rope.layer[j] = gp.attn.layer[j] = gp.first + j;
-            gp.rope.q[j] = m.q[j]; gp.rope.k[j] = m.k[j]; gp.rope.v[j] = m.v[j];
-            gp.attn.q[j] = m.q[j]; gp.attn.out[j] = m.a[j];
+            if (full)
+                for (int j = 0; j < n; ++j) {
+                    const Layer& y = m.ly[l0 + j];
+                    GvOp& o = b.op(m.F, m.s[j], m.F, GEPI_SWIGLU);
+                    b.seg(o, y.wg, m.d, xm[j], 0);
+                    b.seg(o, y.wu, m.d, xm[j], 1);
+                }
+            if (pre.njobs) out.push_back(norm_rec(pre, M));
+            out.push_back(finish_gv(c, b, full ? "gv_qkv_gateup" : "gv_qkv"));
         }
+        out.push_back(attn_rec(c, m, l0, n, M));
         if (full) {
             // K-concatenated [Wo_1 .. Wo_n, Wdown_1 .. Wdown_n] . [a_1..a_n, s_1..s_n]
-            GemvOp kc = make_op(m.d, m.h, m.d, EPI_ACC);
-            for (int j = 0; j < n; ++j) add_seg(kc, m.ly[gp.first + j].wo, m.a[j], m.qd, m.qd);
-            for (int j = 0; j < n; ++j) add_seg(kc, m.ly[gp.first + j].wd, m.s[j], m.F, m.F);
-            gp.kcat = upload_ops(c, {kc});
-            gp.n_mlp = 0;
-        } else {
-            std::vector<GemvOp> os;
+            GvBuild b(M, m.eps, m.esz, !fast);
+            int xa[MAX_GROUP], xs[MAX_GROUP];
+            for (int j = 0; j < n; ++j) xa[j] = raw(b, m.a[j], m.qd);
+            for (int j = 0; j < n; ++j) xs[j] = raw(b, m.s[j], m.F);
+            GvOp& o = b.op(m.d, m.h, m.d, GEPI_ACC);
+            for (int j = 0; j < n; ++j) b.seg(o, m.ly[l0 + j].wo, m.qd, xa[j], 0);
+            for (int j = 0; j < n; ++j) b.seg(o, m.ly[l0 + j].wd, m.F, xs[j], 0);
+            out.push_back(finish_gv(c, b, "gv_o_down_kcat"));
+            continue;
+        }
+        // output projections: exact layer accumulates into h; an
+        // attention-only set stores A_j for the sequential MLPs below
+        {
+            GvBuild b(M, m.eps, m.esz, !fast);
             for (int j = 0; j < n; ++j) {
-                // exact layer: o accumulates into h; ATTN_ONLY set: A_j stored
-                GemvOp o = gp.fuzzy ? make_op(m.d, m.A[j], m.d, EPI_STORE) : make_op(m.d, m.h, m.d, EPI_ACC);
-                add_seg(o, m.ly[gp.first + j].wo, m.a[j], m.qd, m.qd);
-                os.push_back(o);
+                const int xa = raw(b, m.a[j], m.qd);
+                GvOp& o = fuzzy ? b.op(m.d, m.A[j], m.d, GEPI_STORE) : b.op(m.d, m.h, m.d, GEPI_ACC);
+                b.seg(o, m.ly[l0 + j].wo, m.qd, xa, 0);
             }
-            gp.o = upload_ops(c, os);
-            gp.n_mlp = n;
-            for (int j = 0; j < n; ++j) {
-                const Layer& y = m.ly[gp.first + j];
-                gp.norm_mlp[j] = norm_args(m, m.h, gp.fuzzy ? m.A[j] : nullptr);
-                add_job(gp.norm_mlp[j], y.mn, m.mb[0]);
-                GemvOp sw = make_op(m.F, m.s[0], m.F, EPI_SWIGLU);
-                add_seg(sw, y.wg, m.mb[0], m.d, m.d);
-                add_seg(sw, y.wu, m.mb[0], m.d, m.d);
-                gp.swi[j] = upload_ops(c, {sw});
-                GemvOp dn = make_op(m.d, m.h, m.d, EPI_ACC);
-                add_seg(dn, y.wd, m.s[0], m.F, m.F);
-                gp.down[j] = upload_ops(c, {dn});
+            out.push_back(finish_gv(c, b, "gv_o"));
+        }
+        for (int j = 0; j < n; ++j) {
+            const Layer& y = m.ly[l0 + j];
+            const float* add = fuzzy ? m.A[j] : nullptr;  // x = h + A_j before this MLP
+            bool fused = false;
+            {
+                GvBuild b(M, m.eps, m.esz, !fast);
+                NormArgs pre = norm_args(m, m.h, nullptr);
+                const int xm = norm_source(b, pre, y.mn, m.mb[0], add, &fused);
+                GvOp& o = b.op(m.F, m.s[0], m.F, GEPI_SWIGLU);
+                b.seg(o, y.wg, m.d, xm, 0);
+                b.seg(o, y.wu, m.d, xm, 1);
+                if (pre.njobs) out.push_back(norm_rec(pre, M));
+                out.push_back(finish_gv(c, b, "gv_gateup"));
+            }
+            {
+                GvBuild b(M, m.eps, m.esz, !fast);
+                const int xs = raw(b, m.s[0], m.F);
+                // with a fused norm h does not hold A_j yet: add it here
+                GvOp& o = (add && fused) ? b.op(m.d, m.h, m.d, GEPI_ACC_ADD, add) : b.op(m.d, m.h, m.d, GEPI_ACC);
+                b.seg(o, y.wd, m.F, xs, 0);
+                out.push_back(finish_gv(c, b, "gv_down"));
             }
         }
-        plan.push_back(gp);
     }
-    return plan;
+    return out;
+}
+
+// Output head: final RMSNorm of rows r*stride + off of h, logits into
+// y + r*ldy.
+std::vector<Rec> build_head(es_ctx* c, Model& m, int rows, int stride, int off, float* y, int ldy) {
+    const bool fast = rows <= GV_MAXM;
+    std::vector<Rec> out;
+    GvBuild b(rows, m.eps, m.esz, !fast);
+    int xs = fast ? b.source(m.h, nullptr, m.fnorm, m.d, m.d, stride, off, XS_NORM) : -1;
+    if (xs < 0) {
+        NormArgs a = norm_args(m, m.h, nullptr);
+        a.src_stride = stride; a.src_off = off;
+        add_job(a, m.fnorm, m.xf);
+        out.push_back(norm_rec(a, rows));
+        xs = b.source(m.xf, nullptr, nullptr, m.d, m.d, 1, 0, XS_RAW);
+    }
+    b.seg(b.op(m.V, y, ldy, GEPI_STORE), m.lm, m.d, xs, 0);
+    out.push_back(finish_gv(c, b, "gv_lm_head"));
+    return out;
 }
 
 std::vector<std::vector<int>> default_sets(int L, int k) {
@@ -449,128 +549,60 @@ std::vector<std::vector<int>> default_sets(int L, int k) {
 
 // ------------------------------------------------------------------ launches
 template <typename T>
-void run_gemv(es_ctx* c, const GemvLaunch& gl, int M) {
-    if (gl.nops == 0 || M <= 0) return;
-    const int block = GEMV_WARPS * 32;
-    if (M <= 8) {
-        const int grid = std::min(gl.gemv_tiles, c->num_sms * 6);
-        switch (M) {
-#define ES_GEMV_CASE(MM) \
-    case MM: launch(c, "gemv_m" #MM, gl.bytes(M), gemv_kernel<T, MM>, dim3(grid), dim3(block), gl.ops, gl.nops, gl.gemv_tiles); break;
-            ES_GEMV_CASE(1) ES_GEMV_CASE(2) ES_GEMV_CASE(3) ES_GEMV_CASE(4)
-            ES_GEMV_CASE(5) ES_GEMV_CASE(6) ES_GEMV_CASE(7) ES_GEMV_CASE(8)
-#undef ES_GEMV_CASE
-        }
-    } else {
-        launch(c, "gemm_simt", gl.bytes(M), gemm_kernel<T>, dim3(gl.gemm_tiles, (M + GB - 1) / GB), dim3(256),
-               gl.ops + gl.nops, gl.nops, M);
+void run_rec(es_ctx* c, const Rec& r) {
+    switch (r.kind) {
+        case R_GV:
+            switch (r.M) {
+#define ES_GV_CASE(MM)                                                                              \
+    case MM:                                                                                        \
+        launch(c, r.name, r.bytes, gv_kernel<T, MM>, dim3(r.grid), dim3(GV_THREADS), (size_t)r.smem, \
+               r.gv, c->gv_scratch, c->gv_counters);                                     \
+        break;
+                ES_GV_CASE(1) ES_GV_CASE(2) ES_GV_CASE(3) ES_GV_CASE(4)
+                ES_GV_CASE(5) ES_GV_CASE(6) ES_GV_CASE(7) ES_GV_CASE(8)
+#undef ES_GV_CASE
+                default: arg_fail(ES_ERR_ARG, "internal: GEMV rows %d", r.M);
+            }
+            break;
+        case R_GEMM:
+            launch(c, "gemm_simt", r.bytes, gemm_kernel<T>, dim3(r.ntiles64, (r.M + GB - 1) / GB), dim3(256),
+                   (size_t)0, r.gv);
+            break;
+        case R_NORM:
+            launch(c, r.name, 0.0, norm_kernel<T>, dim3(r.M), dim3(256), (size_t)0, r.norm);
+            break;
+        default:
+            launch(c, r.name, 0.0, attn_kernel<T>, r.g3, dim3(ATT_THREADS), (size_t)r.smem, r.attn);
+            break;
     }
 }
 
+// Embedding of the rows described by `kind` (or by the host), then the
+// planned forward.
 template <typename T>
-void run_norm(es_ctx* c, const NormArgs& a, int rows) {
-    launch(c, "rmsnorm", 0.0, norm_kernel<T>, dim3(rows), dim3(256), a);
-}
-
-template <typename T>
-void run_group(es_ctx* c, Model& m, const GroupPlan& gp, int M) {
-    run_norm<T>(c, gp.norm_in, M);
-    run_gemv<T>(c, gp.wide, M);
-    RopeArgs r = gp.rope; r.M = M;
-    launch(c, "rope_kv", 0.0, rope_kv_kernel<T>, dim3(M, gp.n), dim3(128), r);
-    AttnArgs a = gp.attn; a.M = M;
-    launch(c, "attn_split", 0.0, attn_split_kernel<T>, dim3(M, gp.n * m.Hkv, m.nsplit), dim3(128), a);
-    launch(c, "attn_combine", 0.0, attn_combine_kernel, dim3(M, gp.n, m.H), dim3(std::max(32, (m.hd + 31) / 32 * 32)), a);
-    if (gp.kcat.nops) {
-        run_gemv<T>(c, gp.kcat, M);
-        return;
-    }
-    run_gemv<T>(c, gp.o, M);
-    for (int j = 0; j < gp.n_mlp; ++j) {
-        run_norm<T>(c, gp.norm_mlp[j], M);
-        run_gemv<T>(c, gp.swi[j], M);
-        run_gemv<T>(c, gp.down[j], M);
-    }
-}
-
-// Body of one forward pass over M rows already described by the row arrays
-// (or described by `kind` on the device).
-template <typename T>
-void run_forward(es_ctx* c, Model& m, const std::vector<GroupPlan>& plan, int kind, int step,
-                 int gamma, int M) {
-    launch(c, "prep_embed", 0.0, prep_embed_kernel<T>, dim3(M), dim3(256), kind, step, gamma, M,
+void run_forward(es_ctx* c, Model& m, const std::vector<Rec>& plan, int kind, int step, int gamma, int M) {
+    launch(c, "prep_embed", 0.0, prep_embed_kernel<T>, dim3(M), dim3(256), (size_t)0, kind, step, gamma, M,
            (const int*)c->n_commit, (const int*)c->tokens, c->cfg.max_seq, (const int*)c->dtok,
-           c->cfg.max_gamma, m.row_pos, m.row_seq, m.row_tok, (const T*)m.embed, m.h, m.d, m.V,
+           c->cfg.max_gamma, m.row_pos, m.row_seq, m.row_tok, m.row_base, (const T*)m.embed, m.h, m.d, m.V,
            c->status);
-    for (const auto& gp : plan) run_group<T>(c, m, gp, M);
+    for (const Rec& r : plan) run_rec<T>(c, r);
 }
 
-// Head: final norm of the selected rows and the output projection.
-template <typename T>
-void run_head(es_ctx* c, Model& m, int rows, int src_stride, int src_off, const GemvLaunch& lm) {
-    NormArgs a = norm_args(m, m.h, nullptr);
-    a.src_stride = src_stride; a.src_off = src_off;
-    add_job(a, m.fnorm, m.xf);
-    run_norm<T>(c, a, rows);
-    run_gemv<T>(c, lm, rows);
-}
-
-const GemvLaunch& head_desc(es_ctx* c, Model& m, int gamma, int kind, int step) {
-    auto key = std::make_tuple(gamma, kind, step);
-    auto it = c->heads.find(key);
-    if (it != c->heads.end()) return it->second;
-    GemvOp op;
-    if (kind == KIND_VERIFY) op = make_op(m.V, c->p_logits, m.V, EPI_STORE);
-    else op = make_op(m.V, c->q_logits + (size_t)step * m.V, gamma * m.V, EPI_STORE);
-    add_seg(op, m.lm, m.xf, m.d, m.d);
-    c->cur_esz = m.esz;
-    return c->heads[key] = upload_ops(c, {op});
-}
-
-// ------------------------------------------------------------------ phase parts
-template <typename TD>
-void enqueue_calibrate(es_ctx* c, const std::vector<GroupPlan>& exact_d, int gamma) {
-    Model& m = c->md;
-    const int B = c->B;
-    const GemvLaunch& lm = head_desc(c, m, gamma, KIND_CALIB, 0);
-    run_forward<TD>(c, m, exact_d, KIND_CALIB, 0, gamma, B * (gamma + 1));
-    run_head<TD>(c, m, B, gamma + 1, gamma, lm);
-    launch(c, "softmax_sample", 0.0, softmax_sample_kernel, dim3(B), dim3(1024), (const float*)c->q_logits, c->q_probs, m.V,
-           1, 0, gamma, (const RunParams*)c->prm, (const int64_t*)c->phase, gamma, c->dtok,
-           c->cfg.max_gamma);
-}
-
-template <typename TD>
-void enqueue_fuzzy(es_ctx* c, const std::vector<GroupPlan>& plan, int gamma) {
-    Model& m = c->md;
-    const int B = c->B;
-    for (int i = 1; i < gamma; ++i) {
-        const GemvLaunch& lm = head_desc(c, m, gamma, KIND_FUZZY, i);
-        run_forward<TD>(c, m, plan, KIND_FUZZY, i, gamma, B);
-        run_head<TD>(c, m, B, 1, 0, lm);
-        launch(c, "softmax_sample", 0.0, softmax_sample_kernel, dim3(B), dim3(1024), (const float*)c->q_logits, c->q_probs,
-               m.V, 1, i, gamma, (const RunParams*)c->prm, (const int64_t*)c->phase, gamma, c->dtok,
-               c->cfg.max_gamma);
-    }
-}
-
-template <typename TB>
-void enqueue_verify(es_ctx* c, const std::vector<GroupPlan>& exact_b, int gamma) {
-    Model& m = c->mb;
-    const int B = c->B, M = B * (gamma + 1);
-    const GemvLaunch& lm = head_desc(c, m, gamma, KIND_VERIFY, 0);
-    run_forward<TB>(c, m, exact_b, KIND_VERIFY, 0, gamma, M);
-    run_head<TB>(c, m, M, 1, 0, lm);
-    launch(c, "softmax", 0.0, softmax_sample_kernel, dim3(M), dim3(1024), (const float*)c->p_logits, c->p_probs, m.V,
-           gamma + 1, 0, gamma + 1, (const RunParams*)c->prm, (const int64_t*)c->phase, gamma,
-           (int*)nullptr, c->cfg.max_gamma);
-    AcceptArgs a;
+// Softmax over rows of logits (and a draw per row when dtok is set).
+void run_softmax(es_ctx* c, const float* z, float* p, int V, int rows, int per_seq, int off, int ld_rows,
+                 int gamma, int* dtok) {
+    SampleArgs a;
     memset(&a, 0, sizeof a);
-    a.p = c->p_probs; a.q = c->q_probs; a.d = c->dtok; a.gmax = c->cfg.max_gamma; a.gamma = gamma;
-    a.V = m.V; a.greedy = -1; a.u_explicit = nullptr; a.prm = c->prm; a.phase = c->phase;
-    a.n_acc = c->n_acc; a.out_tok = c->out_tok; a.tokens = c->tokens; a.max_seq = c->cfg.max_seq;
-    a.n_commit = c->n_commit; a.n_limit = c->n_limit;
-    launch(c, "accept_resample", 0.0, accept_kernel, dim3(B), dim3(1024), a);
+    a.z = z; a.p = p; a.V = V;
+    a.chunk = std::max(512, (V + c->num_sms - 1) / c->num_sms);
+    a.nb = (V + a.chunk - 1) / a.chunk;
+    a.per_seq = per_seq; a.off = off; a.ld_rows = ld_rows;
+    a.prm = c->prm; a.phase = c->phase; a.gamma = gamma; a.dtok = dtok; a.gmax = c->cfg.max_gamma;
+    a.part = c->sm_part; a.mass = c->sm_mass; a.counters = c->sm_counters;
+    if (rows > c->sm_rows_cap || a.nb > c->sm_nb_cap) arg_fail(ES_ERR_ARG, "internal: softmax launch too large");
+    launch(c, "softmax_part", 0.0, softmax_part_kernel, dim3(rows, a.nb), dim3(SM_THREADS), (size_t)0, a);
+    launch(c, dtok ? "softmax_sample" : "softmax", 0.0, softmax_finish_kernel, dim3(rows, a.nb),
+           dim3(SM_THREADS), (size_t)0, a);
 }
 
 }  // namespace
@@ -614,11 +646,16 @@ void check_status(es_ctx* c) {
     }
 }
 
-const std::vector<GroupPlan>& get_plan(es_ctx* c, int key) {
-    auto it = c->plans.find(key);
+// ------------------------------------------------------------------ plans
+// Set keys: -1 base (exact), 1 draft exact, 0 draft explicit sets, k >= 2
+// draft sets of size k by the default rule.
+const std::vector<Rec>& get_plan(es_ctx* c, int key, int M) {
+    const int which = key == -1 ? 1 : 0;
+    auto pk = std::make_tuple(which, key, M);
+    auto it = c->plans.find(pk);
     if (it != c->plans.end()) return it->second;
     std::vector<std::vector<int>> sets;
-    Model& m = (key == -1) ? c->mb : c->md;
+    Model& m = which ? c->mb : c->md;
     if (key == -1 || key == 1) {
         sets = default_sets(m.L, 1);
     } else if (key == 0) {
@@ -632,8 +669,58 @@ const std::vector<GroupPlan>& get_plan(es_ctx* c, int key) {
     } else {
         sets = default_sets(m.L, key);
     }
-    c->cur_esz = m.esz;
-    return c->plans[key] = build_plan(c, m, sets, c->cfg.parallel_mode);
+    return c->plans[pk] = build_forward(c, m, sets, c->cfg.parallel_mode, M);
+}
+
+const std::vector<Rec>& get_head(es_ctx* c, Model& m, int rows, int stride, int off, float* y, int ldy) {
+    const int which = &m == &c->mb ? 1 : 0;
+    auto key = std::make_tuple(which, rows, stride, off, (const float*)y, ldy);
+    auto it = c->heads.find(key);
+    if (it != c->heads.end()) return it->second;
+    return c->heads[key] = build_head(c, m, rows, stride, off, y, ldy);
+}
+
+// ------------------------------------------------------------------ phase parts
+template <typename TD>
+void enqueue_calibrate(es_ctx* c, int gamma) {
+    Model& m = c->md;
+    const int B = c->B, M = B * (gamma + 1);
+    const auto& plan = get_plan(c, 1, M);
+    const auto& head = get_head(c, m, B, gamma + 1, gamma, c->q_logits, gamma * m.V);
+    run_forward<TD>(c, m, plan, KIND_CALIB, 0, gamma, M);
+    for (const Rec& r : head) run_rec<TD>(c, r);
+    run_softmax(c, c->q_logits, c->q_probs, m.V, B, 1, 0, gamma, gamma, c->dtok);
+}
+
+template <typename TD>
+void enqueue_fuzzy(es_ctx* c, int key, int gamma) {
+    Model& m = c->md;
+    const int B = c->B;
+    const auto& plan = get_plan(c, key, B);
+    for (int i = 1; i < gamma; ++i) {
+        const auto& head = get_head(c, m, B, 1, 0, c->q_logits + (size_t)i * m.V, gamma * m.V);
+        run_forward<TD>(c, m, plan, KIND_FUZZY, i, gamma, B);
+        for (const Rec& r : head) run_rec<TD>(c, r);
+        run_softmax(c, c->q_logits, c->q_probs, m.V, B, 1, i, gamma, gamma, c->dtok);
+    }
+}
+
+template <typename TB>
+void enqueue_verify(es_ctx* c, int gamma) {
+    Model& m = c->mb;
+    const int B = c->B, M = B * (gamma + 1);
+    const auto& plan = get_plan(c, -1, M);
+    const auto& head = get_head(c, m, M, 1, 0, c->p_logits, m.V);
+    run_forward<TB>(c, m, plan, KIND_VERIFY, 0, gamma, M);
+    for (const Rec& r : head) run_rec<TB>(c, r);
+    run_softmax(c, c->p_logits, c->p_probs, m.V, M, gamma + 1, 0, gamma + 1, gamma, nullptr);
+    AcceptArgs a;
+    memset(&a, 0, sizeof a);
+    a.p = c->p_probs; a.q = c->q_probs; a.d = c->dtok; a.gmax = c->cfg.max_gamma; a.gamma = gamma;
+    a.V = m.V; a.greedy = -1; a.u_explicit = nullptr; a.prm = c->prm; a.phase = c->phase;
+    a.n_acc = c->n_acc; a.out_tok = c->out_tok; a.tokens = c->tokens; a.max_seq = c->cfg.max_seq;
+    a.n_commit = c->n_commit; a.n_limit = c->n_limit;
+    launch(c, "accept_resample", 0.0, accept_kernel, dim3(B), dim3(1024), (size_t)0, a);
 }
 
 void set_params(es_ctx* c, float T, uint64_t seed) {
@@ -645,14 +732,14 @@ void set_params(es_ctx* c, float T, uint64_t seed) {
 template <typename TD, typename TB>
 void enqueue_part(es_ctx* c, int part, int gamma, int k) {
     if (part == 0) {
-        enqueue_calibrate<TD>(c, get_plan(c, 1), gamma);
-        enqueue_fuzzy<TD>(c, get_plan(c, k), gamma);
+        enqueue_calibrate<TD>(c, gamma);
+        enqueue_fuzzy<TD>(c, k, gamma);
     } else if (part == 1) {
-        enqueue_verify<TB>(c, get_plan(c, -1), gamma);
+        enqueue_verify<TB>(c, gamma);
     } else if (part == 2) {
-        enqueue_calibrate<TD>(c, get_plan(c, 1), gamma);
+        enqueue_calibrate<TD>(c, gamma);
     } else {
-        enqueue_fuzzy<TD>(c, get_plan(c, k), gamma);
+        enqueue_fuzzy<TD>(c, k, gamma);
     }
 }
 
@@ -669,15 +756,22 @@ void dispatch_part(es_ctx* c, int part, int gamma, int k) {
 // (part, gamma, k, B) as a CUDA graph and replayed.
 void run_part(es_ctx* c, int part, int gamma, int k) {
     // build every descriptor before capture (uploads are synchronous)
-    if (part != 1) { get_plan(c, 1); get_plan(c, k); }
-    else get_plan(c, -1);
-    for (int i = 0; i < gamma; ++i) head_desc(c, c->md, gamma, i == 0 ? KIND_CALIB : KIND_FUZZY, i);
-    head_desc(c, c->mb, gamma, KIND_VERIFY, 0);
+    const int B = c->B;
+    if (part != 1) {
+        get_plan(c, 1, B * (gamma + 1));
+        get_plan(c, k, B);
+        get_head(c, c->md, B, gamma + 1, gamma, c->q_logits, gamma * c->md.V);
+        for (int i = 1; i < gamma; ++i)
+            get_head(c, c->md, B, 1, 0, c->q_logits + (size_t)i * c->md.V, gamma * c->md.V);
+    } else {
+        get_plan(c, -1, B * (gamma + 1));
+        get_head(c, c->mb, B * (gamma + 1), 1, 0, c->p_logits, c->mb.V);
+    }
     if (c->profiling) {  // eager launches, each bracketed by events
         dispatch_part(c, part, gamma, k);
         return;
     }
-    auto key = std::make_tuple(part, gamma, k, c->B);
+    auto key = std::make_tuple(part, gamma, k, B);
     auto it = c->graphs.find(key);
     if (it == c->graphs.end()) {
         cudaGraph_t g;
@@ -708,26 +802,30 @@ template <typename T>
 void prefill_model(es_ctx* c, Model& m, const int32_t* prompts, int B, int P) {
     // exact forward over positions 0..P-2 of every sequence, in chunks of
     // positions (rows of a chunk only attend to earlier positions)
-    const auto& plan = (&m == &c->mb) ? get_plan(c, -1) : get_plan(c, 1);
     const int npos = P - 1;
     if (npos <= 0) return;
+    const int key = (&m == &c->mb) ? -1 : 1;
     const int chunk = std::max(1, m.Mw / B);
-    std::vector<int> pos, seq, tok;
+    std::vector<int> pos, seq, tok, base;
     for (int p0 = 0; p0 < npos; p0 += chunk) {
         const int p1 = std::min(npos, p0 + chunk);
-        pos.clear(); seq.clear(); tok.clear();
+        pos.clear(); seq.clear(); tok.clear(); base.clear();
         for (int b = 0; b < B; ++b)
             for (int p = p0; p < p1; ++p) {
                 pos.push_back(p); seq.push_back(b); tok.push_back(prompts[(size_t)b * P + p]);
+                base.push_back(b * (p1 - p0));
             }
         const int M = (int)pos.size();
+        const auto& plan = get_plan(c, key, M);
         CK(cudaMemcpyAsync(m.row_pos, pos.data(), M * sizeof(int), cudaMemcpyHostToDevice, c->st));
         CK(cudaMemcpyAsync(m.row_seq, seq.data(), M * sizeof(int), cudaMemcpyHostToDevice, c->st));
         CK(cudaMemcpyAsync(m.row_tok, tok.data(), M * sizeof(int), cudaMemcpyHostToDevice, c->st));
+        CK(cudaMemcpyAsync(m.row_base, base.data(), M * sizeof(int), cudaMemcpyHostToDevice, c->st));
         run_forward<T>(c, m, plan, KIND_HOST, 0, 0, M);
         CK(cudaStreamSynchronize(c->st));  // host row buffers are reused
     }
 }
+
 
 void do_prefill(es_ctx* c, const int32_t* prompts, int B, int P) {
     if (!prompts || B < 1 || P < 1) arg_fail(ES_ERR_ARG, "prefill: need prompts, B >= 1, P >= 1");
@@ -892,8 +990,28 @@ es_status easyspec_init(const es_config* cfg, const es_weights* draft, const es_
         c->p_probs = c->dalloc<float>((size_t)Bm * (G + 1) * V);
         c->prm = c->dalloc<RunParams>(1);
         c->status = c->dalloc<int>(1);
-        c->arena_cap = 1 << 14;
-        c->arena = c->dalloc<GemvOp>(c->arena_cap);
+        c->arena_cap = (size_t)64 << 20;
+        c->arena = c->dalloc<char>(c->arena_cap);
+        c->gv_scratch = c->dalloc<float>(GV_SCRATCH_FLOATS);
+        c->gv_counters = c->dalloc<int>(GV_COUNTERS);
+        c->att_counters = c->dalloc<int>(ATT_COUNTERS);
+        c->sm_rows_cap = std::max(c->md.Mw, c->mb.Mw);
+        c->sm_nb_cap = c->num_sms + 1;
+        c->sm_part = c->dalloc<float>((size_t)c->sm_rows_cap * c->sm_nb_cap * 2);
+        c->sm_mass = c->dalloc<unsigned long long>((size_t)c->sm_rows_cap * c->sm_nb_cap);
+        c->sm_counters = c->dalloc<int>(c->sm_rows_cap);
+        // dynamic shared memory beyond 48 KB must be allowed per kernel
+        const int gv_smem = GV_XSMEM_MAX * (int)sizeof(float);
+#define ES_GV_ATTR(TT, MM) \
+        CK(cudaFuncSetAttribute(gv_kernel<TT, MM>, cudaFuncAttributeMaxDynamicSharedMemorySize, gv_smem));
+        ES_GV_ATTR(bf16, 1) ES_GV_ATTR(bf16, 2) ES_GV_ATTR(bf16, 3) ES_GV_ATTR(bf16, 4)
+        ES_GV_ATTR(bf16, 5) ES_GV_ATTR(bf16, 6) ES_GV_ATTR(bf16, 7) ES_GV_ATTR(bf16, 8)
+        ES_GV_ATTR(float, 1) ES_GV_ATTR(float, 2) ES_GV_ATTR(float, 3) ES_GV_ATTR(float, 4)
+        ES_GV_ATTR(float, 5) ES_GV_ATTR(float, 6) ES_GV_ATTR(float, 7) ES_GV_ATTR(float, 8)
+#undef ES_GV_ATTR
+        const int att_smem = (int)attn_smem_bytes(MAX_GQA, 256);
+        CK(cudaFuncSetAttribute(attn_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, att_smem));
+        CK(cudaFuncSetAttribute(attn_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, att_smem));
         CK(cudaMallocHost(&c->h_prm, sizeof(RunParams)));
         CK(cudaMallocHost(&c->h_small, sizeof(int) * (64 + 64 * 17 + 64)));
         CK(cudaDeviceSynchronize());
