@@ -24,7 +24,7 @@ namespace es {
 constexpr int PAGE = 64;          // KV page: 64 positions
 constexpr int MAX_GROUP = 8;      // layers per fused set
 constexpr int MAX_GQA = 16;       // query heads per kv head
-constexpr int ATT_THREADS = 128;
+constexpr int ATT_THREADS = 256;
 constexpr int ATT_COUNTERS = 16384;
 
 // Paged cache: element (page p, layer l, K|V, kv head h, slot s, e) at
@@ -49,9 +49,10 @@ struct AttnArgs {
     const int* row_pos; const int* row_seq; const int* row_base;
 };
 
-// dynamic shared memory (floats): qs G*(hd+4) | ks 64*(hd+4) | vs 64*(hd+4) | sc G*64
-inline size_t attn_smem_bytes(int G, int hd) {
-    return sizeof(float) * ((size_t)G * (hd + 4) + 2 * 64 * (hd + 4) + (size_t)G * 64);
+// dynamic shared memory (floats): qs G*(hd+4) | ks 64*(hd+4) | vs 64*(hd+4) |
+// sc G*max(64, nsplit) (scores, then the split-merge weights)
+inline size_t attn_smem_bytes(int G, int hd, int nsplit) {
+    return sizeof(float) * ((size_t)G * (hd + 4) + 2 * 64 * (hd + 4) + (size_t)G * (nsplit > 64 ? nsplit : 64));
 }
 
 template <typename T>
@@ -75,29 +76,57 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_kernel(AttnArgs a) {
     const float scale = 1.0f / sqrtf((float)hd);
     const int kvd = Hkv * hd, qd = a.H * hd;
 
-    // rotated, scaled queries of the G heads at this row's position
-    {
-        const float* q = a.q[j] + (size_t)m * qd + (size_t)hk * G * hd;
-        const float* cs = a.rope + (size_t)pos * hd;
-        for (int t = tid; t < G * half; t += ATT_THREADS) {
-            const int h = t / half, i = t % half;
-            const float c = cs[2 * i], s = cs[2 * i + 1];
-            const float x0 = q[h * hd + i], x1 = q[h * hd + i + half];
-            qs[h * ld + i] = (x0 * c - x1 * s) * scale;
-            qs[h * ld + i + half] = (x1 * c + x0 * s) * scale;
+    const bool cached = p0 + n <= bpos;  // every position of this split is in the cache
+    // Issue the independent global loads together: the cached K/V page of
+    // this split (16-byte vectors), the queries and their rotation factors.
+    constexpr int EPV = 16 / sizeof(T);
+    constexpr int VPT = 8;  // vectors of K (and of V) per thread and pass
+    const int nv = n * hd / EPV;
+    const T* Kp = kv_ptr<T>(a.g, seq, p0, layer, 0, hk);
+    const T* Vp = kv_ptr<T>(a.g, seq, p0, layer, 1, hk);
+    const float* q = a.q[j] + (size_t)m * qd + (size_t)hk * G * hd;
+    const float* csq = a.rope + (size_t)pos * hd;
+    for (int base = 0; base < (cached ? nv : 0) || base == 0; base += VPT * ATT_THREADS) {
+        uint4 kv4[VPT], vv4[VPT];
+        if (cached) {
+#pragma unroll
+            for (int u = 0; u < VPT; ++u) {
+                const int t = base + u * ATT_THREADS + tid;
+                if (t < nv) {
+                    kv4[u] = *reinterpret_cast<const uint4*>(Kp + (size_t)t * EPV);
+                    vv4[u] = *reinterpret_cast<const uint4*>(Vp + (size_t)t * EPV);
+                }
+            }
         }
+        if (base == 0) {
+            for (int t = tid; t < G * half; t += ATT_THREADS) {
+                const int h = t / half, i = t % half;
+                const float c = csq[2 * i], sn = csq[2 * i + 1];
+                const float x0 = q[h * hd + i], x1 = q[h * hd + i + half];
+                qs[h * ld + i] = (x0 * c - x1 * sn) * scale;
+                qs[h * ld + i + half] = (x1 * c + x0 * sn) * scale;
+            }
+        }
+        if (cached) {
+#pragma unroll
+            for (int u = 0; u < VPT; ++u) {
+                const int t = base + u * ATT_THREADS + tid;
+                if (t < nv) {
+                    float kf[EPV], vf[EPV];
+                    unpack16(kv4[u], kf, T());
+                    unpack16(vv4[u], vf, T());
+                    const int i = t * EPV / hd, e = t * EPV % hd;
+#pragma unroll
+                    for (int x = 0; x < EPV; ++x) { ks[i * ld + e + x] = kf[x]; vs[i * ld + e + x] = vf[x]; }
+                }
+            }
+        }
+        if (!cached) break;
     }
-    // keys and values of positions p0 .. p0+n-1
-    if (p0 + n <= bpos) {
-        // all from the cache: contiguous [n][hd] blocks of this page
-        const T* Kp = kv_ptr<T>(a.g, seq, p0, layer, 0, hk);
-        const T* Vp = kv_ptr<T>(a.g, seq, p0, layer, 1, hk);
-        for (int t = tid; t < n * hd; t += ATT_THREADS) {
-            const int i = t / hd, e = t % hd;
-            ks[i * ld + e] = to_f32(Kp[t]);
-            vs[i * ld + e] = to_f32(Vp[t]);
-        }
-    } else {
+    if (!cached) {
+        // the split holding this launch's own rows: cached positions before
+        // bpos, the launch's raw k/v rows (rotated, rounded to the cache
+        // type as a cached entry would be) from bpos on
         for (int t = tid; t < n * half; t += ATT_THREADS) {
             const int i = t / half, e = t % half, p = p0 + i;
             float k0, k1, v0, v1;
@@ -107,14 +136,12 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_kernel(AttnArgs a) {
                 k0 = to_f32(kr[e]); k1 = to_f32(kr[e + half]);
                 v0 = to_f32(vr[e]); v1 = to_f32(vr[e + half]);
             } else {
-                // this launch's own row for position p: rotate, then round
-                // to the cache type exactly as a cached entry would be
                 const size_t r = (size_t)(rb + (p - bpos)) * kvd + (size_t)hk * hd;
                 const float* cs = a.rope + (size_t)p * hd;
-                const float c = cs[2 * e], s = cs[2 * e + 1];
+                const float c = cs[2 * e], sn = cs[2 * e + 1];
                 const float x0 = a.k[j][r + e], x1 = a.k[j][r + e + half];
-                k0 = to_f32(from_f32<T>(x0 * c - x1 * s));
-                k1 = to_f32(from_f32<T>(x1 * c + x0 * s));
+                k0 = to_f32(from_f32<T>(x0 * c - x1 * sn));
+                k1 = to_f32(from_f32<T>(x1 * c + x0 * sn));
                 v0 = to_f32(from_f32<T>(a.v[j][r + e]));
                 v1 = to_f32(from_f32<T>(a.v[j][r + e + half]));
             }
@@ -133,12 +160,12 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_kernel(AttnArgs a) {
             vd[e] = from_f32<T>(vs[i * ld + e]);
         }
     }
-    // scores: thread -> (position i, every other head)
+    // scores: thread -> (position i, every fourth head)
     {
         const int i = tid % PAGE, hp = tid / PAGE;
         if (i < n) {
             const float* kr = ks + i * ld;
-            for (int h = hp; h < G; h += 2) {
+            for (int h = hp; h < G; h += ATT_THREADS / PAGE) {
                 const float* qh = qs + h * ld;
                 float s = 0.f;
                 for (int e = 0; e < hd; e += 4) {
@@ -189,19 +216,37 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_kernel(AttnArgs a) {
     __syncthreads();
     if (!s_last) return;
     __threadfence();
+    // merge weights w[h][p] = exp(m_p - max) / sum_p' exp(m_p' - max) l_p'
+    // (reusing the score buffer: nact <= nsplit splits per head)
+    float* wsm = sc;
+    for (int t = tid; t < G * nact; t += ATT_THREADS) {
+        const int h = t / nact, p = t % nact;
+        wsm[h * a.nsplit + p] = __ldcg(part_row + ((size_t)h * a.nsplit + p) * (hd + 2) + hd);
+    }
+    __syncthreads();
+    for (int h = warp; h < G; h += ATT_THREADS / 32) {
+        float mx = -INFINITY;
+        for (int p = lane; p < nact; p += 32) mx = fmaxf(mx, wsm[h * a.nsplit + p]);
+        mx = warp_max(mx);
+        float den = 0.f;
+        for (int p = lane; p < nact; p += 32) {
+            const float w = expf(wsm[h * a.nsplit + p] - mx);
+            wsm[h * a.nsplit + p] = w;
+            den = fmaf(w, __ldcg(part_row + ((size_t)h * a.nsplit + p) * (hd + 2) + hd + 1), den);
+        }
+        den = warp_sum(den);
+        const float inv = 1.0f / den;
+        for (int p = lane; p < nact; p += 32) wsm[h * a.nsplit + p] *= inv;
+    }
+    __syncthreads();
     for (int t = tid; t < G * hd; t += ATT_THREADS) {
         const int h = t / hd, e = t % hd;
-        const float* pp = part_row + (size_t)h * a.nsplit * (hd + 2);
-        float mx = -INFINITY;
-        for (int p = 0; p < nact; ++p) mx = fmaxf(mx, __ldcg(pp + (size_t)p * (hd + 2) + hd));
-        float num = 0.f, den = 0.f;
-        for (int p = 0; p < nact; ++p) {
-            const float* q = pp + (size_t)p * (hd + 2);
-            const float w = expf(__ldcg(q + hd) - mx);
-            den = fmaf(w, __ldcg(q + hd + 1), den);
-            num = fmaf(w, __ldcg(q + e), num);
-        }
-        outp[t] = num / den;
+        const float* pp = part_row + (size_t)h * a.nsplit * (hd + 2) + e;
+        const float* wh = wsm + h * a.nsplit;
+        float num = 0.f;
+#pragma unroll 4
+        for (int p = 0; p < nact; ++p) num = fmaf(wh[p], __ldcg(pp + (size_t)p * (hd + 2)), num);
+        outp[t] = num;
     }
     if (tid == 0) *ctr = 0;
 }

@@ -48,11 +48,19 @@ struct Rec {
     int kind = R_GV;
     const char* name = "";
     double bytes = 0;          // algorithmic bytes (weights + activations), 0 if not modelled
-    const GvLaunch* gv = nullptr;
+    const GvLaunch* gv = nullptr;           // device copy (after upload)
+    std::shared_ptr<GvLaunch> host;         // host copy while the plan is built
     int grid = 0, smem = 0, M = 0, ntiles64 = 0;
     NormArgs norm{};
     AttnArgs attn{};
     dim3 g3;
+};
+
+// A planned forward pass: the embedding kernel's normalisation jobs for the
+// first weight pass, then the launches.
+struct Plan {
+    GvPost first{};
+    std::vector<Rec> recs;
 };
 
 struct ProfRec { const char* name; double bytes; cudaEvent_t a, b; };
@@ -67,7 +75,7 @@ struct Model {
     KVGeom g{};
     float* rope = nullptr;
     int slots = 1, Mw = 0, nsplit = 0;
-    float *h = nullptr, *xf = nullptr, *part = nullptr;
+    float *h = nullptr, *xf = nullptr, *part = nullptr, *rinv = nullptr;
     std::vector<float*> xb, mb, q, k, v, a, s, A;
     int *row_pos = nullptr, *row_seq = nullptr, *row_tok = nullptr, *row_base = nullptr;
 };
@@ -100,6 +108,7 @@ struct es_ctx {
     // scratch of the split kernels (partials and arrival counters)
     float* gv_scratch = nullptr;
     int* gv_counters = nullptr;
+    int* gv_done = nullptr;
     int* att_counters = nullptr;
     float* sm_part = nullptr;
     unsigned long long* sm_mass = nullptr;
@@ -130,9 +139,7 @@ struct es_ctx {
     std::map<std::string, ProfAgg> prof;
 
     // planned forwards: key (model 0 draft / 1 base, set key, rows)
-    std::map<std::tuple<int, int, int>, std::vector<Rec>> plans;
-    // planned output heads: key (model, rows, row stride, row offset, y, ldy)
-    std::map<std::tuple<int, int, int, int, const float*, int>, std::vector<Rec>> heads;
+    std::map<std::tuple<int, int, int, int, int, int>, Plan> plans;
     std::map<std::tuple<int, int, int, int>, Graph> graphs;  // (part, gamma, k, B)
 
     template <typename T>
@@ -269,6 +276,7 @@ void setup_model(es_ctx* c, Model& m, const es_model_shape& s, const es_weights*
     const size_t Mw = m.Mw;
     m.h = c->dalloc<float>(Mw * m.d);
     m.xf = c->dalloc<float>(Mw * m.d);
+    m.rinv = c->dalloc<float>(Mw);
     for (int j = 0; j < slots; ++j) {
         m.xb.push_back(c->dalloc<float>(Mw * m.d));
         m.mb.push_back(c->dalloc<float>(Mw * m.d));
@@ -290,45 +298,59 @@ void setup_model(es_ctx* c, Model& m, const es_model_shape& s, const es_weights*
 // ------------------------------------------------------------------ GEMV launch building
 // Collects the ops and activation sources of one weight-streaming launch.
 struct GvBuild {
-    GvLaunch L;
+    std::shared_ptr<GvLaunch> L;
     size_t esz;
     int xfloats = 0;
     bool simt;  // many-row launch (SIMT GEMM): every source read from global memory
-    GvBuild(int M, float eps, size_t esz_, bool simt_) : esz(esz_), simt(simt_) {
-        memset(&L, 0, sizeof L);
-        L.M = M;
-        L.eps = eps;
+    GvBuild(int M, size_t esz_, bool simt_) : L(std::make_shared<GvLaunch>()), esz(esz_), simt(simt_) {
+        memset(L.get(), 0, sizeof(GvLaunch));
+        L->M = M;
     }
-    // Register an activation source; -1 when a normalised source does not
-    // fit in shared memory (the caller then normalises it beforehand).
-    int source(const float* src, const float* add, const void* gain, int K, int ld, int rs, int ro,
-               int kind) {
-        if (L.nxs >= GV_MAX_XS) arg_fail(ES_ERR_ARG, "too many activation sources in one launch");
-        const int need = L.M * K;
+    // An activation source: rows r*rs + ro of src (leading dimension ld).
+    // Staged in shared memory while room is left, else read from global.
+    int source(const float* src, int K, int ld, int rs = 1, int ro = 0) {
+        if (L->nxs >= GV_MAX_XS) arg_fail(ES_ERR_ARG, "too many activation sources in one launch");
+        const int need = L->M * K;
         int off = -1;
         if (!simt && xfloats + need <= GV_XSMEM_MAX) { off = xfloats; xfloats += (need + 3) & ~3; }
-        if (kind == XS_NORM && off < 0) return -1;
-        GvXSrc& x = L.xs[L.nxs];
-        x.src = src; x.add = add; x.gain = gain; x.K = K; x.ld = ld; x.row_stride = rs; x.row_off = ro;
-        x.kind = kind; x.smem_off = off;
-        return L.nxs++;
+        GvXSrc& x = L->xs[L->nxs];
+        x.src = src; x.K = K; x.ld = ld; x.row_stride = rs; x.row_off = ro; x.smem_off = off; x.kind = XS_RAW;
+        return L->nxs++;
     }
-    GvOp& op(int N, float* y, int ldy, int epi, const float* add = nullptr) {
-        if (L.nops >= GV_MAX_OPS) arg_fail(ES_ERR_ARG, "too many ops in one launch");
-        GvOp& o = L.ops[L.nops++];
+    // A normalised source (h + add) * rinv * gain, rows r*rs + ro of h; -1
+    // when it does not fit in shared memory (the caller normalises it first).
+    int norm_source(const float* h, const float* add, const void* gain, const float* rinv, int K, int rs, int ro) {
+        if (simt || xfloats + L->M * K > GV_XSMEM_MAX) return -1;
+        const int i = source(h, K, K, rs, ro);
+        GvXSrc& x = L->xs[i];
+        x.kind = XS_NORM; x.add = add; x.gain = gain; x.rinv = rinv;
+        return i;
+    }
+    int op(int N, float* y, int ldy, int epi, const float* add = nullptr) {
+        if (L->nops >= GV_MAX_OPS) arg_fail(ES_ERR_ARG, "too many ops in one launch");
+        GvOp& o = L->ops[L->nops];
         o.N = N; o.y = y; o.ldy = ldy; o.epi = epi; o.add = add;
-        return o;
+        o.seg0 = 0; o.nseg = 0;
+        return L->nops++;
     }
-    void seg(GvOp& o, const void* W, int K, int xs, int set) {
-        if (o.nseg >= GV_MAX_SEG) arg_fail(ES_ERR_ARG, "too many K-concatenated segments");
-        if (xs < 0 || L.xs[xs].K != K) arg_fail(ES_ERR_ARG, "segment / source width mismatch");
-        GvSeg& s = o.seg[o.nseg++];
+    // segments of an op must be added right after the op, in order
+    void seg(int oi, const void* W, int K, int xs, int set) {
+        GvOp& o = L->ops[oi];
+        int nsegs = 0;
+        for (int i = 0; i < L->nops; ++i) nsegs += L->ops[i].nseg;
+        if (o.nseg == 0) o.seg0 = nsegs;
+        if (o.seg0 + o.nseg != nsegs) arg_fail(ES_ERR_ARG, "internal: segments out of order");
+        if (o.nseg >= GV_MAX_SEG || nsegs >= GV_MAX_SEGS) arg_fail(ES_ERR_ARG, "too many K-concatenated segments");
+        if (xs < 0 || L->xs[xs].K != K) arg_fail(ES_ERR_ARG, "segment / source width mismatch");
+        GvSeg& s = L->segs[nsegs];
         s.W = W; s.K = K; s.xs = xs; s.set = set;
+        o.nseg++;
     }
 };
 
+// Stage bookkeeping; the descriptor stays on the host until upload_plan().
 Rec finish_gv(es_ctx* c, GvBuild& b, const char* name) {
-    GvLaunch& L = b.L;
+    GvLaunch& L = *b.L;
     const int SC = GV_ROW_BYTES / (int)b.esz;
     int t = 0, st = 0, t64 = 0;
     double wbytes = 0, rowbytes = 0;
@@ -336,20 +358,27 @@ Rec finish_gv(es_ctx* c, GvBuild& b, const char* name) {
         GvOp& o = L.ops[i];
         o.spt = 0;
         for (int s = 0; s < o.nseg; ++s) {
-            o.seg[s].nck = (o.seg[s].K + SC - 1) / SC;
-            o.spt += o.seg[s].nck;
-            wbytes += (double)o.N * o.seg[s].K * b.esz;
+            GvSeg& sg = L.segs[o.seg0 + s];
+            sg.nck = (sg.K + SC - 1) / SC;
+            o.spt += sg.nck;
+            wbytes += (double)o.N * sg.K * b.esz;
         }
         o.ntiles = (o.N + GV_RT - 1) / GV_RT;
         o.tile0 = t; o.stage0 = st; o.tile64_0 = t64;
         t += o.ntiles; st += o.ntiles * o.spt; t64 += (o.N + GB - 1) / GB;
         rowbytes += (double)o.N * 4.0 * (o.epi == GEPI_STORE || o.epi == GEPI_SWIGLU ? 1 : o.epi == GEPI_ACC ? 2 : 3);
     }
-    for (int i = 0; i < L.nxs; ++i) rowbytes += (double)L.xs[i].K * 4.0 * (L.xs[i].add ? 2 : 1);
+    for (int i = 0; i < L.nxs; ++i) rowbytes += (double)L.xs[i].K * 4.0;
     L.ntiles = t; L.nstages = st; L.ntiles64 = t64;
     const int ctas = c->num_sms * GV_CTAS_PER_SM;
     L.q = std::max(1, (st + ctas - 1) / ctas);
     L.x_smem_floats = b.xfloats;
+    int items = 0;  // staging items (4 columns of one row) of the shared-memory sources
+    for (int i = 0; i < L.nxs; ++i) {
+        L.xs[i].item0 = items;
+        if (L.xs[i].smem_off >= 0) items += L.M * (L.xs[i].K / 4);
+    }
+    L.x_items = items;
     if (t > GV_COUNTERS) arg_fail(ES_ERR_ARG, "launch has %d tiles (> %d)", t, GV_COUNTERS);
     Rec r;
     r.kind = b.simt ? R_GEMM : R_GV;
@@ -359,14 +388,21 @@ Rec finish_gv(es_ctx* c, GvBuild& b, const char* name) {
     r.smem = b.xfloats * (int)sizeof(float);
     r.ntiles64 = t64;
     r.bytes = wbytes + L.M * rowbytes;
-    // upload the used prefix of the descriptor
-    const size_t bytes = offsetof(GvLaunch, ops) + (size_t)L.nops * sizeof(GvOp);
-    const size_t at = (c->arena_used + 255) & ~(size_t)255;
-    if (at + bytes > c->arena_cap) arg_fail(ES_ERR_OOM, "launch descriptor arena exhausted");
-    CK(cudaMemcpy(c->arena + at, &L, bytes, cudaMemcpyHostToDevice));
-    c->arena_used = at + bytes;
-    r.gv = reinterpret_cast<const GvLaunch*>(c->arena + at);
+    r.host = b.L;
     return r;
+}
+
+void upload_plan(es_ctx* c, Plan& p) {
+    for (Rec& r : p.recs) {
+        if (!r.host) continue;
+        const size_t bytes = sizeof(GvLaunch);
+        const size_t at = (c->arena_used + 255) & ~(size_t)255;
+        if (at + bytes > c->arena_cap) arg_fail(ES_ERR_OOM, "launch descriptor arena exhausted");
+        CK(cudaMemcpy(c->arena + at, r.host.get(), bytes, cudaMemcpyHostToDevice));
+        c->arena_used = at + bytes;
+        r.gv = reinterpret_cast<const GvLaunch*>(c->arena + at);
+        r.host.reset();
+    }
 }
 
 NormArgs norm_args(Model& m, float* h, const float* add) {
@@ -401,49 +437,69 @@ Rec attn_rec(es_ctx* c, Model& m, int l0, int n, int M) {
     a.part = m.part; a.counters = c->att_counters;
     a.row_pos = m.row_pos; a.row_seq = m.row_seq; a.row_base = m.row_base;
     r.g3 = dim3(M, n * m.Hkv, m.nsplit);
-    r.smem = (int)attn_smem_bytes(m.H / m.Hkv, m.hd);
+    r.smem = (int)attn_smem_bytes(m.H / m.Hkv, m.hd, m.nsplit);
+    if (r.smem > 200 * 1024) arg_fail(ES_ERR_ARG, "attention needs %d bytes of shared memory (max_seq too large)", r.smem);
     r.M = M;
     return r;
 }
 
+// Output head of a forward pass: logits of rows r*stride + off of h into
+// y + r*ldy.
+struct HeadSpec { int rows = 0, stride = 1, off = 0, ldy = 0; float* y = nullptr; };
+
 // Plan of one forward pass over M rows for the layer sets `groups` (sets of
-// one layer are exact layers).  M <= GV_MAXM: fused weight-streaming launches
-// (norms inside the GEMV, RoPE and KV append inside attention); larger M:
-// explicit norm launches and the SIMT GEMM.
-std::vector<Rec> build_forward(es_ctx* c, Model& m, const std::vector<std::vector<int>>& groups,
-                               int mode, int M) {
-    const bool fast = M <= GV_MAXM;
-    std::vector<Rec> out;
-    // an activation RMSNorm(h [+ add]) * gain: fused when it fits, else a
-    // norm launch (which also folds `add` into h) writes it to `buf`;
-    // returns the source index and whether it was fused
-    auto norm_source = [&](GvBuild& b, NormArgs& pre, const void* gain, float* buf,
-                           const float* add, bool* fused) -> int {
+// one layer are exact layers), followed by the output head when
+// head.rows > 0.  M <= GV_MAXM: fused weight-streaming launches; each
+// launch's normalised inputs are produced by the launch before it (the
+// embedding kernel for the first), RoPE and the KV append happen inside
+// attention.  Larger M: explicit norm launches and the SIMT GEMM.
+Plan build_forward(es_ctx* c, Model& m, const std::vector<std::vector<int>>& groups, int mode, int M,
+                   const HeadSpec& head) {
+    const bool fast = M <= GV_MAXM && head.rows <= GV_MAXM;
+    Plan P;
+    // -- fused path: attach a normalisation to the launch that runs just before
+    //    its consumer
+    int writer = -1;  // index in P.recs of the last weight launch (-1: embedding)
+    // 1/rms of the rows the next launch normalises, computed at the end of
+    // the launch before it
+    auto request = [&](const float* add, int rows, int stride, int off) {
+        GvPost& p = writer < 0 ? P.first : P.recs[writer].host->post;
+        if (p.rows) arg_fail(ES_ERR_ARG, "internal: two normalisations after one launch");
+        p.h = m.h; p.add = add; p.rinv = m.rinv; p.rows = rows; p.row_stride = stride; p.row_off = off;
+        p.K = m.d; p.eps = m.eps;
+    };
+    // a normalised input of the launch being built: fused into its staging
+    // when it fits, else written beforehand by a norm launch (which also
+    // folds `add` into h) into `buf`
+    auto norm_input = [&](GvBuild& b, NormArgs& pre, const void* gain, float* buf, const float* add,
+                          int rs, int ro, bool* fused) -> int {
         if (fast) {
-            const int xs = b.source(m.h, add, gain, m.d, m.d, 1, 0, XS_NORM);
+            const int xs = b.norm_source(m.h, add, gain, m.rinv, m.d, rs, ro);
             if (xs >= 0) { if (fused) *fused = true; return xs; }
         }
         if (fused) *fused = false;
-        if (pre.add != add && pre.njobs) arg_fail(ES_ERR_ARG, "internal: mixed norm inputs");
-        pre.add = add;
+        pre.add = add; pre.src_stride = rs; pre.src_off = ro;
         add_job(pre, gain, buf);
-        return b.source(buf, nullptr, nullptr, m.d, m.d, 1, 0, XS_RAW);
+        return b.source(buf, m.d, m.d);
     };
-    auto raw = [&](GvBuild& b, const float* p, int K) {
-        return b.source(p, nullptr, nullptr, K, K, 1, 0, XS_RAW);
+    auto push_gv = [&](GvBuild& b, const char* name) {
+        P.recs.push_back(finish_gv(c, b, name));
+        writer = (int)P.recs.size() - 1;
     };
+    auto raw = [&](GvBuild& b, const float* p, int K) { return b.source(p, K, K); };
     for (const auto& gl : groups) {
         const int n = (int)gl.size(), l0 = gl.front();
         if (n > m.slots || n > MAX_GROUP) arg_fail(ES_ERR_ARG, "layer set larger than %d", MAX_GROUP);
         const bool fuzzy = n > 1, full = fuzzy && mode == ES_FULL_LAYER;
         // ---- wide pass: q, k, v of every layer (+ SwiGLU of every layer)
         {
-            GvBuild b(M, m.eps, m.esz, !fast);
+            if (fast) request(nullptr, M, 1, 0);
+            GvBuild b(M, m.esz, !fast);
             NormArgs pre = norm_args(m, m.h, nullptr);
             int xa[MAX_GROUP], xm[MAX_GROUP];
-            for (int j = 0; j < n; ++j) xa[j] = norm_source(b, pre, m.ly[l0 + j].an, m.xb[j], nullptr, nullptr);
+            for (int j = 0; j < n; ++j) xa[j] = norm_input(b, pre, m.ly[l0 + j].an, m.xb[j], nullptr, 1, 0, nullptr);
             if (full)
-                for (int j = 0; j < n; ++j) xm[j] = norm_source(b, pre, m.ly[l0 + j].mn, m.mb[j], nullptr, nullptr);
+                for (int j = 0; j < n; ++j) xm[j] = norm_input(b, pre, m.ly[l0 + j].mn, m.mb[j], nullptr, 1, 0, nullptr);
             for (int j = 0; j < n; ++j) {
                 const Layer& y = m.ly[l0 + j];
                 b.seg(b.op(m.qd, m.q[j], m.qd, GEPI_STORE), y.wq, m.d, xa[j], 0);
@@ -453,81 +509,73 @@ std::vector<Rec> build_forward(es_ctx* c, Model& m, const std::vector<std::vecto
             if (full)
                 for (int j = 0; j < n; ++j) {
                     const Layer& y = m.ly[l0 + j];
-                    GvOp& o = b.op(m.F, m.s[j], m.F, GEPI_SWIGLU);
+                    const int o = b.op(m.F, m.s[j], m.F, GEPI_SWIGLU);
                     b.seg(o, y.wg, m.d, xm[j], 0);
                     b.seg(o, y.wu, m.d, xm[j], 1);
                 }
-            if (pre.njobs) out.push_back(norm_rec(pre, M));
-            out.push_back(finish_gv(c, b, full ? "gv_qkv_gateup" : "gv_qkv"));
+            if (pre.njobs) P.recs.push_back(norm_rec(pre, M));
+            push_gv(b, full ? "gv_qkv_gateup" : "gv_qkv");
         }
-        out.push_back(attn_rec(c, m, l0, n, M));
+        P.recs.push_back(attn_rec(c, m, l0, n, M));
         if (full) {
             // K-concatenated [Wo_1 .. Wo_n, Wdown_1 .. Wdown_n] . [a_1..a_n, s_1..s_n]
-            GvBuild b(M, m.eps, m.esz, !fast);
+            GvBuild b(M, m.esz, !fast);
             int xa[MAX_GROUP], xs[MAX_GROUP];
             for (int j = 0; j < n; ++j) xa[j] = raw(b, m.a[j], m.qd);
             for (int j = 0; j < n; ++j) xs[j] = raw(b, m.s[j], m.F);
-            GvOp& o = b.op(m.d, m.h, m.d, GEPI_ACC);
+            const int o = b.op(m.d, m.h, m.d, GEPI_ACC);
             for (int j = 0; j < n; ++j) b.seg(o, m.ly[l0 + j].wo, m.qd, xa[j], 0);
             for (int j = 0; j < n; ++j) b.seg(o, m.ly[l0 + j].wd, m.F, xs[j], 0);
-            out.push_back(finish_gv(c, b, "gv_o_down_kcat"));
+            push_gv(b, "gv_o_down_kcat");
             continue;
         }
-        // output projections: exact layer accumulates into h; an
+        // output projections: an exact layer accumulates into h; an
         // attention-only set stores A_j for the sequential MLPs below
         {
-            GvBuild b(M, m.eps, m.esz, !fast);
+            GvBuild b(M, m.esz, !fast);
             for (int j = 0; j < n; ++j) {
                 const int xa = raw(b, m.a[j], m.qd);
-                GvOp& o = fuzzy ? b.op(m.d, m.A[j], m.d, GEPI_STORE) : b.op(m.d, m.h, m.d, GEPI_ACC);
+                const int o = fuzzy ? b.op(m.d, m.A[j], m.d, GEPI_STORE) : b.op(m.d, m.h, m.d, GEPI_ACC);
                 b.seg(o, m.ly[l0 + j].wo, m.qd, xa, 0);
             }
-            out.push_back(finish_gv(c, b, "gv_o"));
+            push_gv(b, "gv_o");
         }
         for (int j = 0; j < n; ++j) {
             const Layer& y = m.ly[l0 + j];
-            const float* add = fuzzy ? m.A[j] : nullptr;  // x = h + A_j before this MLP
+            const float* add = fuzzy ? m.A[j] : nullptr;  // this MLP's input is h + A_j
             bool fused = false;
             {
-                GvBuild b(M, m.eps, m.esz, !fast);
+                if (fast) request(add, M, 1, 0);
+                GvBuild b(M, m.esz, !fast);
                 NormArgs pre = norm_args(m, m.h, nullptr);
-                const int xm = norm_source(b, pre, y.mn, m.mb[0], add, &fused);
-                GvOp& o = b.op(m.F, m.s[0], m.F, GEPI_SWIGLU);
+                const int xm = norm_input(b, pre, y.mn, m.mb[0], add, 1, 0, &fused);
+                const int o = b.op(m.F, m.s[0], m.F, GEPI_SWIGLU);
                 b.seg(o, y.wg, m.d, xm, 0);
                 b.seg(o, y.wu, m.d, xm, 1);
-                if (pre.njobs) out.push_back(norm_rec(pre, M));
-                out.push_back(finish_gv(c, b, "gv_gateup"));
+                if (pre.njobs) P.recs.push_back(norm_rec(pre, M));
+                push_gv(b, "gv_gateup");
             }
             {
-                GvBuild b(M, m.eps, m.esz, !fast);
+                GvBuild b(M, m.esz, !fast);
                 const int xs = raw(b, m.s[0], m.F);
-                // with a fused norm h does not hold A_j yet: add it here
-                GvOp& o = (add && fused) ? b.op(m.d, m.h, m.d, GEPI_ACC_ADD, add) : b.op(m.d, m.h, m.d, GEPI_ACC);
+                // with the fused norm h does not hold A_j yet: add it here
+                const int o = (add && fused) ? b.op(m.d, m.h, m.d, GEPI_ACC_ADD, add) : b.op(m.d, m.h, m.d, GEPI_ACC);
                 b.seg(o, y.wd, m.F, xs, 0);
-                out.push_back(finish_gv(c, b, "gv_down"));
+                push_gv(b, "gv_down");
             }
         }
     }
-    return out;
-}
-
-// Output head: final RMSNorm of rows r*stride + off of h, logits into
-// y + r*ldy.
-std::vector<Rec> build_head(es_ctx* c, Model& m, int rows, int stride, int off, float* y, int ldy) {
-    const bool fast = rows <= GV_MAXM;
-    std::vector<Rec> out;
-    GvBuild b(rows, m.eps, m.esz, !fast);
-    int xs = fast ? b.source(m.h, nullptr, m.fnorm, m.d, m.d, stride, off, XS_NORM) : -1;
-    if (xs < 0) {
-        NormArgs a = norm_args(m, m.h, nullptr);
-        a.src_stride = stride; a.src_off = off;
-        add_job(a, m.fnorm, m.xf);
-        out.push_back(norm_rec(a, rows));
-        xs = b.source(m.xf, nullptr, nullptr, m.d, m.d, 1, 0, XS_RAW);
+    if (head.rows > 0) {
+        if (fast) request(nullptr, head.rows, head.stride, head.off);
+        GvBuild b(head.rows, m.esz, !fast);
+        NormArgs pre = norm_args(m, m.h, nullptr);
+        const int xs = norm_input(b, pre, m.fnorm, m.xf, nullptr, head.stride, head.off, nullptr);
+        b.seg(b.op(m.V, head.y, head.ldy, GEPI_STORE), m.lm, m.d, xs, 0);
+        if (pre.njobs) P.recs.push_back(norm_rec(pre, head.rows));
+        push_gv(b, "gv_lm_head");
     }
-    b.seg(b.op(m.V, y, ldy, GEPI_STORE), m.lm, m.d, xs, 0);
-    out.push_back(finish_gv(c, b, "gv_lm_head"));
-    return out;
+    upload_plan(c, P);
+    return P;
 }
 
 std::vector<std::vector<int>> default_sets(int L, int k) {
@@ -556,7 +604,7 @@ void run_rec(es_ctx* c, const Rec& r) {
 #define ES_GV_CASE(MM)                                                                              \
     case MM:                                                                                        \
         launch(c, r.name, r.bytes, gv_kernel<T, MM>, dim3(r.grid), dim3(GV_THREADS), (size_t)r.smem, \
-               r.gv, c->gv_scratch, c->gv_counters);                                     \
+               r.gv, c->gv_scratch, c->gv_counters, c->gv_done);                                    \
         break;
                 ES_GV_CASE(1) ES_GV_CASE(2) ES_GV_CASE(3) ES_GV_CASE(4)
                 ES_GV_CASE(5) ES_GV_CASE(6) ES_GV_CASE(7) ES_GV_CASE(8)
@@ -578,14 +626,20 @@ void run_rec(es_ctx* c, const Rec& r) {
 }
 
 // Embedding of the rows described by `kind` (or by the host), then the
-// planned forward.
+// planned forward (and its head, if planned).
 template <typename T>
-void run_forward(es_ctx* c, Model& m, const std::vector<Rec>& plan, int kind, int step, int gamma, int M) {
+void run_forward(es_ctx* c, Model& m, const Plan& plan, int kind, int step, int gamma, int M) {
     launch(c, "prep_embed", 0.0, prep_embed_kernel<T>, dim3(M), dim3(256), (size_t)0, kind, step, gamma, M,
            (const int*)c->n_commit, (const int*)c->tokens, c->cfg.max_seq, (const int*)c->dtok,
            c->cfg.max_gamma, m.row_pos, m.row_seq, m.row_tok, m.row_base, (const T*)m.embed, m.h, m.d, m.V,
-           c->status);
-    for (const Rec& r : plan) run_rec<T>(c, r);
+           c->status, plan.first);
+    for (const Rec& r : plan.recs) run_rec<T>(c, r);
+}
+
+// Vocabulary chunks of the softmax / draw / accept kernels: about one per SM.
+void vocab_chunks(int V, int num_sms, int* chunk, int* nb) {
+    *chunk = std::max(512, (V + num_sms - 1) / num_sms);
+    *nb = (V + *chunk - 1) / *chunk;
 }
 
 // Softmax over rows of logits (and a draw per row when dtok is set).
@@ -593,9 +647,8 @@ void run_softmax(es_ctx* c, const float* z, float* p, int V, int rows, int per_s
                  int gamma, int* dtok) {
     SampleArgs a;
     memset(&a, 0, sizeof a);
-    a.z = z; a.p = p; a.V = V;
-    a.chunk = std::max(512, (V + c->num_sms - 1) / c->num_sms);
-    a.nb = (V + a.chunk - 1) / a.chunk;
+    a.z = z; a.p = p; a.V = V; a.greedy = -1;
+    vocab_chunks(V, c->num_sms, &a.chunk, &a.nb);
     a.per_seq = per_seq; a.off = off; a.ld_rows = ld_rows;
     a.prm = c->prm; a.phase = c->phase; a.gamma = gamma; a.dtok = dtok; a.gmax = c->cfg.max_gamma;
     a.part = c->sm_part; a.mass = c->sm_mass; a.counters = c->sm_counters;
@@ -648,10 +701,13 @@ void check_status(es_ctx* c) {
 
 // ------------------------------------------------------------------ plans
 // Set keys: -1 base (exact), 1 draft exact, 0 draft explicit sets, k >= 2
-// draft sets of size k by the default rule.
-const std::vector<Rec>& get_plan(es_ctx* c, int key, int M) {
+// draft sets of size k by the default rule.  Heads: 0 none, 1 calibration
+// (last row of each sequence -> q slot 0), 2 fuzzy step (-> q slot step),
+// 3 verify (every row -> p).
+enum { HEAD_NONE = 0, HEAD_CALIB = 1, HEAD_FUZZY = 2, HEAD_VERIFY = 3 };
+const Plan& get_forward(es_ctx* c, int key, int M, int head_kind, int step, int gamma) {
     const int which = key == -1 ? 1 : 0;
-    auto pk = std::make_tuple(which, key, M);
+    auto pk = std::make_tuple(which, key, M, head_kind, step, gamma);
     auto it = c->plans.find(pk);
     if (it != c->plans.end()) return it->second;
     std::vector<std::vector<int>> sets;
@@ -669,15 +725,12 @@ const std::vector<Rec>& get_plan(es_ctx* c, int key, int M) {
     } else {
         sets = default_sets(m.L, key);
     }
-    return c->plans[pk] = build_forward(c, m, sets, c->cfg.parallel_mode, M);
-}
-
-const std::vector<Rec>& get_head(es_ctx* c, Model& m, int rows, int stride, int off, float* y, int ldy) {
-    const int which = &m == &c->mb ? 1 : 0;
-    auto key = std::make_tuple(which, rows, stride, off, (const float*)y, ldy);
-    auto it = c->heads.find(key);
-    if (it != c->heads.end()) return it->second;
-    return c->heads[key] = build_head(c, m, rows, stride, off, y, ldy);
+    HeadSpec h;
+    const int B = c->B;
+    if (head_kind == HEAD_CALIB) { h.rows = B; h.stride = gamma + 1; h.off = gamma; h.y = c->q_logits; h.ldy = gamma * m.V; }
+    if (head_kind == HEAD_FUZZY) { h.rows = B; h.y = c->q_logits + (size_t)step * m.V; h.ldy = gamma * m.V; }
+    if (head_kind == HEAD_VERIFY) { h.rows = M; h.y = c->p_logits; h.ldy = m.V; }
+    return c->plans[pk] = build_forward(c, m, sets, c->cfg.parallel_mode, M, h);
 }
 
 // ------------------------------------------------------------------ phase parts
@@ -685,10 +738,7 @@ template <typename TD>
 void enqueue_calibrate(es_ctx* c, int gamma) {
     Model& m = c->md;
     const int B = c->B, M = B * (gamma + 1);
-    const auto& plan = get_plan(c, 1, M);
-    const auto& head = get_head(c, m, B, gamma + 1, gamma, c->q_logits, gamma * m.V);
-    run_forward<TD>(c, m, plan, KIND_CALIB, 0, gamma, M);
-    for (const Rec& r : head) run_rec<TD>(c, r);
+    run_forward<TD>(c, m, get_forward(c, 1, M, HEAD_CALIB, 0, gamma), KIND_CALIB, 0, gamma, M);
     run_softmax(c, c->q_logits, c->q_probs, m.V, B, 1, 0, gamma, gamma, c->dtok);
 }
 
@@ -696,11 +746,8 @@ template <typename TD>
 void enqueue_fuzzy(es_ctx* c, int key, int gamma) {
     Model& m = c->md;
     const int B = c->B;
-    const auto& plan = get_plan(c, key, B);
     for (int i = 1; i < gamma; ++i) {
-        const auto& head = get_head(c, m, B, 1, 0, c->q_logits + (size_t)i * m.V, gamma * m.V);
-        run_forward<TD>(c, m, plan, KIND_FUZZY, i, gamma, B);
-        for (const Rec& r : head) run_rec<TD>(c, r);
+        run_forward<TD>(c, m, get_forward(c, key, B, HEAD_FUZZY, i, gamma), KIND_FUZZY, i, gamma, B);
         run_softmax(c, c->q_logits, c->q_probs, m.V, B, 1, i, gamma, gamma, c->dtok);
     }
 }
@@ -709,18 +756,17 @@ template <typename TB>
 void enqueue_verify(es_ctx* c, int gamma) {
     Model& m = c->mb;
     const int B = c->B, M = B * (gamma + 1);
-    const auto& plan = get_plan(c, -1, M);
-    const auto& head = get_head(c, m, M, 1, 0, c->p_logits, m.V);
-    run_forward<TB>(c, m, plan, KIND_VERIFY, 0, gamma, M);
-    for (const Rec& r : head) run_rec<TB>(c, r);
+    run_forward<TB>(c, m, get_forward(c, -1, M, HEAD_VERIFY, 0, gamma), KIND_VERIFY, 0, gamma, M);
     run_softmax(c, c->p_logits, c->p_probs, m.V, M, gamma + 1, 0, gamma + 1, gamma, nullptr);
     AcceptArgs a;
     memset(&a, 0, sizeof a);
     a.p = c->p_probs; a.q = c->q_probs; a.d = c->dtok; a.gmax = c->cfg.max_gamma; a.gamma = gamma;
     a.V = m.V; a.greedy = -1; a.u_explicit = nullptr; a.prm = c->prm; a.phase = c->phase;
+    vocab_chunks(m.V, c->num_sms, &a.chunk, &a.nb);
+    a.gpart = c->sm_part; a.mass = c->sm_mass; a.counters = c->sm_counters;
     a.n_acc = c->n_acc; a.out_tok = c->out_tok; a.tokens = c->tokens; a.max_seq = c->cfg.max_seq;
     a.n_commit = c->n_commit; a.n_limit = c->n_limit;
-    launch(c, "accept_resample", 0.0, accept_kernel, dim3(B), dim3(1024), (size_t)0, a);
+    launch(c, "accept_resample", 0.0, accept_kernel, dim3(B, a.nb), dim3(SM_THREADS), (size_t)0, a);
 }
 
 void set_params(es_ctx* c, float T, uint64_t seed) {
@@ -755,17 +801,13 @@ void dispatch_part(es_ctx* c, int part, int gamma, int k) {
 // 2 = calibration only, 3 = fuzzy drafts only.  Captured once per
 // (part, gamma, k, B) as a CUDA graph and replayed.
 void run_part(es_ctx* c, int part, int gamma, int k) {
-    // build every descriptor before capture (uploads are synchronous)
-    const int B = c->B;
+    // build every plan before capture (descriptor uploads are synchronous)
+    const int B = c->B, M = B * (gamma + 1);
     if (part != 1) {
-        get_plan(c, 1, B * (gamma + 1));
-        get_plan(c, k, B);
-        get_head(c, c->md, B, gamma + 1, gamma, c->q_logits, gamma * c->md.V);
-        for (int i = 1; i < gamma; ++i)
-            get_head(c, c->md, B, 1, 0, c->q_logits + (size_t)i * c->md.V, gamma * c->md.V);
+        get_forward(c, 1, M, HEAD_CALIB, 0, gamma);
+        for (int i = 1; i < gamma; ++i) get_forward(c, k, B, HEAD_FUZZY, i, gamma);
     } else {
-        get_plan(c, -1, B * (gamma + 1));
-        get_head(c, c->mb, B * (gamma + 1), 1, 0, c->p_logits, c->mb.V);
+        get_forward(c, -1, M, HEAD_VERIFY, 0, gamma);
     }
     if (c->profiling) {  // eager launches, each bracketed by events
         dispatch_part(c, part, gamma, k);
@@ -816,7 +858,7 @@ void prefill_model(es_ctx* c, Model& m, const int32_t* prompts, int B, int P) {
                 base.push_back(b * (p1 - p0));
             }
         const int M = (int)pos.size();
-        const auto& plan = get_plan(c, key, M);
+        const Plan& plan = get_forward(c, key, M, HEAD_NONE, 0, 0);
         CK(cudaMemcpyAsync(m.row_pos, pos.data(), M * sizeof(int), cudaMemcpyHostToDevice, c->st));
         CK(cudaMemcpyAsync(m.row_seq, seq.data(), M * sizeof(int), cudaMemcpyHostToDevice, c->st));
         CK(cudaMemcpyAsync(m.row_tok, tok.data(), M * sizeof(int), cudaMemcpyHostToDevice, c->st));
@@ -994,11 +1036,12 @@ es_status easyspec_init(const es_config* cfg, const es_weights* draft, const es_
         c->arena = c->dalloc<char>(c->arena_cap);
         c->gv_scratch = c->dalloc<float>(GV_SCRATCH_FLOATS);
         c->gv_counters = c->dalloc<int>(GV_COUNTERS);
+        c->gv_done = c->dalloc<int>(1);
         c->att_counters = c->dalloc<int>(ATT_COUNTERS);
         c->sm_rows_cap = std::max(c->md.Mw, c->mb.Mw);
         c->sm_nb_cap = c->num_sms + 1;
         c->sm_part = c->dalloc<float>((size_t)c->sm_rows_cap * c->sm_nb_cap * 2);
-        c->sm_mass = c->dalloc<unsigned long long>((size_t)c->sm_rows_cap * c->sm_nb_cap);
+        c->sm_mass = c->dalloc<unsigned long long>((size_t)c->sm_rows_cap * c->sm_nb_cap * 2);
         c->sm_counters = c->dalloc<int>(c->sm_rows_cap);
         // dynamic shared memory beyond 48 KB must be allowed per kernel
         const int gv_smem = GV_XSMEM_MAX * (int)sizeof(float);
@@ -1009,7 +1052,7 @@ es_status easyspec_init(const es_config* cfg, const es_weights* draft, const es_
         ES_GV_ATTR(float, 1) ES_GV_ATTR(float, 2) ES_GV_ATTR(float, 3) ES_GV_ATTR(float, 4)
         ES_GV_ATTR(float, 5) ES_GV_ATTR(float, 6) ES_GV_ATTR(float, 7) ES_GV_ATTR(float, 8)
 #undef ES_GV_ATTR
-        const int att_smem = (int)attn_smem_bytes(MAX_GQA, 256);
+        const int att_smem = 200 * 1024;
         CK(cudaFuncSetAttribute(attn_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, att_smem));
         CK(cudaFuncSetAttribute(attn_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, att_smem));
         CK(cudaMallocHost(&c->h_prm, sizeof(RunParams)));
@@ -1150,15 +1193,43 @@ es_status es_accept_resample(const float* p, const float* q, const int32_t* d, c
                              void* stream) {
     if (!p || !q || !d || !n_acc || !tok || B < 1 || gamma < 1 || gamma > 16 || V < 1) return ES_ERR_ARG;
     if (!greedy && !u) return ES_ERR_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    int dev = 0, nsm = 148;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return ES_ERR_CUDA;
     AcceptArgs a;
     memset(&a, 0, sizeof a);
     a.p = p; a.q = q; a.d = d; a.gmax = gamma; a.gamma = gamma; a.V = V; a.greedy = greedy ? 1 : 0;
     a.u_explicit = u; a.n_acc = n_acc; a.out_tok = tok;
-    cudaStream_t st = (cudaStream_t)stream;
-    accept_kernel<<<B, 1024, 0, st>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return ES_ERR_CUDA;
-    if (cudaStreamSynchronize(st) != cudaSuccess) return ES_ERR_CUDA;
-    return ES_OK;
+    vocab_chunks(V, nsm, &a.chunk, &a.nb);
+    // scratch of the split kernels, owned by this call
+    const size_t rows = (size_t)B * (gamma + 1);
+    float* gpart = nullptr;
+    unsigned long long* mass = nullptr;
+    int* ctr = nullptr;
+    es_status rc = ES_OK;
+    if (cudaMalloc(&gpart, rows * a.nb * 2 * sizeof(float)) != cudaSuccess ||
+        cudaMalloc(&mass, (size_t)B * a.nb * 2 * sizeof(unsigned long long)) != cudaSuccess ||
+        cudaMalloc(&ctr, (size_t)B * sizeof(int)) != cudaSuccess ||
+        cudaMemsetAsync(ctr, 0, (size_t)B * sizeof(int), st) != cudaSuccess) {
+        rc = ES_ERR_OOM;
+    } else {
+        a.gpart = gpart; a.mass = mass; a.counters = ctr;
+        if (greedy) {
+            SampleArgs s;
+            memset(&s, 0, sizeof s);
+            s.z = p; s.V = V; s.chunk = a.chunk; s.nb = a.nb; s.per_seq = 1; s.off = 0; s.ld_rows = 1;
+            s.greedy = 1; s.part = gpart;
+            softmax_part_kernel<<<dim3((unsigned)rows, a.nb), SM_THREADS, 0, st>>>(s);
+        }
+        accept_kernel<<<dim3(B, a.nb), SM_THREADS, 0, st>>>(a);
+        if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess) rc = ES_ERR_CUDA;
+    }
+    cudaFree(gpart);
+    cudaFree(mass);
+    cudaFree(ctr);
+    return rc;
 }
 
 es_status es_sample(const float* w, const uint64_t* u, int B, int V, int32_t* idx, void* stream) {

@@ -10,22 +10,27 @@
 //   ACC      y[m][n] += r0                      (residual add)
 //   ACC_ADD  y[m][n] += r0 + add[m][n]          (residual add of two deltas)
 //   SWIGLU   y[m][n]  = silu(r0) * r1
-// Activation inputs ("x sources") are either raw float rows in global memory
-// or RMSNorm(h [+ add]) * gain of a residual row, normalised on the fly while
-// they are staged into shared memory (the norm is fused into the GEMV).
+// Activation sources are plain rows, or normalised rows
+//   x[m] = (h[m*stride + off] + add[...]) * rinv[m] * gain
+// whose reciprocal rms `rinv` was computed by the launch before: after its
+// ops, a launch may run a "post-norm" in which its last CTA to finish writes
+// rinv[r] = 1 / rms(h[r*stride + off] + add[...]) for the next weight pass.
+// So a consumer normalises while it stages its inputs, in the same single
+// pass over memory.
 //
 // Data movement.  A stage is 32 consecutive rows x 512 bytes of one matrix.
-// Each consumer warp owns 4 rows of the 32-row tile and every lane one
-// 16-byte column vector of each, read with 128-bit non-allocating loads
-// straight into registers, several stages ahead (HBM latency is covered by
-// the loads in flight of two resident CTAs per SM), so an activation vector
-// read from shared memory is reused for 4 weight rows.  One-dimensional bulk
-// copies (cp.async.bulk) of 512-byte row pieces into a shared-memory ring
-// were measured on B300 at under 2 TB/s for this access shape, against about
-// 7 TB/s for plain 16-byte loads, so the weights do not go through TMA.
-// Before griddepcontrol.wait every thread prefetches its first weight
-// vectors into L2: they never depend on the previous kernel, so they stream
-// in while that kernel drains.
+// Each warp owns 4 rows of the 32-row tile and every lane one 16-byte column
+// vector of each, read with 128-bit non-allocating loads into registers, the
+// next chunk always requested before the current one is multiplied (two
+// chunks in flight per thread, two CTAs per SM).  An activation vector read
+// from shared memory serves 4 weight rows.  The launch descriptor is copied
+// into shared memory and the first chunk requested before
+// griddepcontrol.wait -- neither depends on the previous kernel -- so both
+// arrive while that kernel drains.  Measured alternatives on B300 for this
+// shape (all slower): TMA tensor tiles (capped near 4.6 TB/s per GPU by the
+// per-SM TMA rate), one-dimensional bulk copies of 512-byte row pieces
+// (under 2 TB/s), cp.async rings, L2 prefetch, and register-fed warp MMA
+// (its 64-byte row pieces per load halve DRAM efficiency).
 //
 // Work split (stream-K).  The launch's stages -- ops, then 32-row tiles,
 // then segments, then 512-byte column chunks -- form one sequence that is cut
@@ -40,51 +45,59 @@
 
 namespace es {
 
-constexpr int GV_WARPS = 8;                    // consumer warps
+constexpr int GV_WARPS = 8;
 constexpr int GV_THREADS = GV_WARPS * 32;
-constexpr int GV_R = 4;                        // rows per consumer warp
+constexpr int GV_R = 4;                        // rows per warp
 constexpr int GV_RT = GV_WARPS * GV_R;         // rows per tile (32)
 constexpr int GV_ROW_BYTES = 512;              // bytes of one row per stage
 constexpr int GV_MAXM = 8;
 constexpr int GV_MAX_XS = 16;
-constexpr int GV_MAX_SEG = 16;
+constexpr int GV_MAX_SEGS = 64;                // segments per launch
+constexpr int GV_MAX_SEG = 16;                 // segments per op
 constexpr int GV_MAX_OPS = 32;
-constexpr int GV_XSMEM_MAX = 24 * 1024;        // floats of staged activations (96 KB)
+constexpr int GV_XSMEM_MAX = 26 * 1024;        // floats of staged activations (104 KB)
 constexpr int GV_CTAS_PER_SM = 2;
 constexpr int GV_SCRATCH_CTAS = 1024;          // partial-sum slots
 constexpr int GV_COUNTERS = 65536;             // arrival counters (tiles per launch)
 constexpr int GV_SCRATCH_FLOATS = GV_SCRATCH_CTAS * 2 * 2 * GV_THREADS;
 
-enum { XS_RAW = 0, XS_NORM = 1 };
 enum { GEPI_STORE = 0, GEPI_ACC = 1, GEPI_ACC_ADD = 2, GEPI_SWIGLU = 3 };
 
+enum { XS_RAW = 0, XS_NORM = 1 };
 // Input row r (< M) of x source i is row r*row_stride + row_off of `src`
-// (leading dimension ld).  NORM: x = (src + add) / rms(src + add) * gain,
-// rms over the K columns; `add` uses the same row mapping and ld.
+// (leading dimension ld).  XS_NORM: x = (src + add) * rinv[r] * gain with the
+// same row mapping for `add`.
 struct GvXSrc {
-    const float* src; const float* add; const void* gain;
+    const float* src; const float* add; const void* gain; const float* rinv;
     int K, ld, row_stride, row_off, kind;
     int smem_off;  // float offset in the staged region, or -1: read from global
+    int item0;     // first staging item (4 columns of one row) of this source
+    int pad_;
 };
 struct GvSeg { const void* W; int K, xs, set, nck; };
 struct GvOp {
-    GvSeg seg[GV_MAX_SEG];
-    int nseg, epi, N, ldy;
     float* y; const float* add;
+    int seg0, nseg, epi, N, ldy;
     int ntiles, spt;       // 32-row tiles, stages per tile
     int tile0, stage0;     // launch-wide tile / stage index of the op's first
-    int tile64_0, pad_;    // (SIMT GEMM) first 64-row tile of the op
+    int tile64_0;          // (SIMT GEMM) first 64-row tile of the op
+};
+// rinv[r] = 1 / sqrt(mean over k < K of (h + add)[r*row_stride + row_off][k]^2
+//                     + eps), h and add with leading dimension K.
+struct GvPost {
+    const float* h; const float* add; float* rinv;
+    int rows, row_stride, row_off, K;
+    float eps; int pad_;
 };
 struct GvLaunch {
-    int nops, nxs, M, ntiles, nstages, q, x_smem_floats, ntiles64;
-    float eps; int pad_;
+    int nops, nxs, M, ntiles, nstages, q, x_smem_floats, ntiles64, x_items, pad_;
     GvXSrc xs[GV_MAX_XS];
     GvOp ops[GV_MAX_OPS];
+    GvSeg segs[GV_MAX_SEGS];
+    GvPost post;
+    int pad2_[2];
 };
-
-// ------------------------------------------------------------ PTX helpers
-ES_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-ES_DEV void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+static_assert(sizeof(GvLaunch) % 16 == 0, "the descriptor is copied in 16-byte pieces");
 
 ES_DEV float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
@@ -102,7 +115,7 @@ struct GvWalk {
         tile = r / o.spt;
         int c = r % o.spt;
         seg = 0;
-        while (c >= o.seg[seg].nck) { c -= o.seg[seg].nck; ++seg; }
+        while (c >= L->segs[o.seg0 + seg].nck) { c -= L->segs[o.seg0 + seg].nck; ++seg; }
         kc = c;
     }
     // advance by n chunks within the current segment (n <= chunks left in
@@ -110,17 +123,7 @@ struct GvWalk {
     ES_DEV bool advance(int n) {
         const GvOp& o = L->ops[op];
         kc += n;
-        if (kc < o.seg[seg].nck) return false;
-        kc = 0;
-        if (++seg < o.nseg) return false;
-        seg = 0;
-        if (++tile >= o.ntiles) { tile = 0; ++op; }
-        return true;
-    }
-    // true when the step crossed into a new tile
-    ES_DEV bool next() {
-        const GvOp& o = L->ops[op];
-        if (++kc < o.seg[seg].nck) return false;
+        if (kc < L->segs[o.seg0 + seg].nck) return false;
         kc = 0;
         if (++seg < o.nseg) return false;
         seg = 0;
@@ -155,9 +158,29 @@ ES_DEV float warp_reduce_scatter(const float (&v)[NV], int lane) {
     return a[0];
 }
 
-// ------------------------------------------------------------ kernel
-ES_DEV void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+// ------------------------------------------------------------ post-norm
+// Executed by one whole CTA (blockDim.x a multiple of 32) once the rows it
+// reads are final: a warp per row.
+ES_DEV void post_rinv(const GvPost& p) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int r = warp; r < p.rows; r += nw) {
+        const size_t base = (size_t)(r * p.row_stride + p.row_off) * p.K;
+        float ss = 0.f;
+#pragma unroll 4
+        for (int k = lane * 4; k < p.K; k += 128) {
+            float4 v = __ldcg(reinterpret_cast<const float4*>(p.h + base + k));
+            if (p.add) {
+                const float4 a = __ldcg(reinterpret_cast<const float4*>(p.add + base + k));
+                v.x += a.x; v.y += a.y; v.z += a.z; v.w += a.w;
+            }
+            ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) p.rinv[r] = 1.0f / sqrtf(ss / (float)p.K + p.eps);
+    }
+}
 
+// ------------------------------------------------------------ kernel
 // acc[r][m] += W-vector(r) . x-vector(m) for one 16-byte column vector.
 template <typename T, int M>
 ES_DEV void gv_fma(const uint4 (&w)[GV_R], const float* __restrict__ x, int xst, float (&acc)[GV_R][M]) {
@@ -180,64 +203,72 @@ ES_DEV void gv_fma(const uint4 (&w)[GV_R], const float* __restrict__ x, int xst,
     }
 }
 
+// The CTA's stage range, walked one chunk at a time.
+struct GvBatch {
+    int op, tile, seg, kc;
+    bool tile_end;   // the chunk completes its tile
+    bool range_end;  // the chunk is the last of this CTA's range
+};
+
 template <typename T, int M>
-__global__ void __launch_bounds__(GV_THREADS, 2)
-gv_kernel(const GvLaunch* __restrict__ L, float* __restrict__ scratch, int* __restrict__ counters) {
+__global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM)
+gv_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __restrict__ counters,
+          int* __restrict__ done) {
     constexpr int EPV = 16 / sizeof(T);            // weights per 16-byte vector
     constexpr int SC = GV_ROW_BYTES / sizeof(T);   // columns per stage: one vector per lane
     constexpr int NV = GV_R * M;
-    constexpr int U = M <= 2 ? 4 : 2;              // stages whose loads are issued together
     extern __shared__ __align__(16) float xsm[];
+    __shared__ __align__(16) GvLaunch L;
     __shared__ const float* xs_base[GV_MAX_XS];
     __shared__ int xs_stride[GV_MAX_XS];
-    __shared__ float xs_rinv[GV_MAX_XS * GV_MAXM];
     __shared__ int s_last;
-
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int Q = L->q;
-    const int s_begin = blockIdx.x * Q;
-    const int s_end = min(L->nstages, s_begin + Q);
 
-    // Weights never depend on the previous kernel: pull this CTA's first
-    // stages into L2 while that kernel drains.
+    // the launch descriptor: one parallel copy into shared memory
     {
-        GvWalk w;
-        w.seek(L, s_begin);
-        const GvOp& o = L->ops[w.op];
-        const GvSeg& sg = o.seg[w.seg];
-        const int n = min(min(s_end - s_begin, 2 * U), sg.nck - w.kc);
+        const int4* src = reinterpret_cast<const int4*>(Lg);
+        int4* dst = reinterpret_cast<int4*>(&L);
+        for (int i = tid; i < (int)(sizeof(GvLaunch) / 16); i += GV_THREADS) dst[i] = src[i];
+    }
+    __syncthreads();
+    const int Q = L.q;
+    const int s_begin = blockIdx.x * Q;
+    const int s_end = min(L.nstages, s_begin + Q);
+
+    GvWalk w;
+    w.seek(&L, s_begin);
+    int s_next = s_begin;
+    auto next_batch = [&](GvBatch& b) -> bool {
+        if (s_next >= s_end) return false;
+        b.op = w.op; b.tile = w.tile; b.seg = w.seg; b.kc = w.kc;
+        b.tile_end = w.advance(1);
+        s_next += 1;
+        b.range_end = s_next == s_end;
+        return true;
+    };
+    auto load = [&](const GvBatch& b, uint4 (&wv)[GV_R]) {
+        const GvOp& o = L.ops[b.op];
+        const GvSeg& sg = L.segs[o.seg0 + b.seg];
+        const int k = b.kc * SC + lane * EPV;
 #pragma unroll
         for (int r = 0; r < GV_R; ++r) {
-            const int row = min(w.tile * GV_RT + warp * GV_R + r, o.N - 1);
-            const T* base = (const T*)sg.W + (size_t)row * sg.K + lane * EPV;
-            for (int u = 0; u < n; ++u)
-                if ((w.kc + u) * SC + lane * EPV < sg.K) prefetch_l2(base + (size_t)(w.kc + u) * SC);
+            // rows past N read the last row; their sums are dropped
+            const T* wr = (const T*)sg.W + (size_t)min(b.tile * GV_RT + warp * GV_R + r, o.N - 1) * sg.K;
+            wv[r] = k < sg.K ? ld_stream16(wr + k) : make_uint4(0u, 0u, 0u, 0u);
         }
-    }
+    };
+
+    // Weights never depend on the previous kernel: request the first chunk
+    // before griddepcontrol.wait.
+    GvBatch cur, nxt;
+    uint4 wc[GV_R], wn[GV_R];
+    bool have = next_batch(cur);
+    if (have) load(cur, wc);
+
     grid_dep_wait();
-    const int nxs = L->nxs;
-    // rms of every normalised source row (warp per row)
-    for (int p = warp; p < nxs * M; p += GV_WARPS) {
-        const int i = p / M, m = p % M;
-        const GvXSrc& x = L->xs[i];
-        if (x.kind != XS_NORM) continue;
-        const size_t r = (size_t)(m * x.row_stride + x.row_off) * x.ld;
-        const float* hr = x.src + r;
-        const float* ar = x.add ? x.add + r : nullptr;
-        float ss = 0.f;
-        for (int k = lane * 4; k < x.K; k += 128) {
-            float4 v = *reinterpret_cast<const float4*>(hr + k);
-            if (ar) {
-                const float4 a = *reinterpret_cast<const float4*>(ar + k);
-                v.x += a.x; v.y += a.y; v.z += a.z; v.w += a.w;
-            }
-            ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-        }
-        ss = warp_sum(ss);
-        if (lane == 0) xs_rinv[p] = 1.0f / sqrtf(ss / (float)x.K + L->eps);
-    }
+    const int nxs = L.nxs;
     if (tid < nxs) {
-        const GvXSrc& x = L->xs[tid];
+        const GvXSrc& x = L.xs[tid];
         if (x.smem_off >= 0) {
             xs_base[tid] = xsm + x.smem_off;
             xs_stride[tid] = x.K;
@@ -246,30 +277,50 @@ gv_kernel(const GvLaunch* __restrict__ L, float* __restrict__ scratch, int* __re
             xs_stride[tid] = x.row_stride * x.ld;
         }
     }
-    __syncthreads();
-    // stage shared-memory sources (normalised ones scaled by rinv * gain)
-    for (int i = 0; i < nxs; ++i) {
-        const GvXSrc& x = L->xs[i];
-        if (x.smem_off < 0) continue;
-        float* dst = xsm + x.smem_off;
-        const int K4 = x.K / 4;
-        for (int t = tid; t < M * K4; t += GV_THREADS) {
-            const int m = t / K4, k = (t % K4) * 4;
-            const size_t r = (size_t)(m * x.row_stride + x.row_off) * x.ld + k;
-            float4 v = *reinterpret_cast<const float4*>(x.src + r);
-            if (x.kind == XS_NORM) {
+    // Stage the shared-memory sources: all (source, row, 4-column) items form
+    // one list; every thread issues the loads of 8 items (activation, added
+    // delta, gain, 1/rms) before using any.
+    const int nitems = L.x_items;
+    constexpr int SB = 8;
+    for (int t0 = tid; t0 < nitems; t0 += SB * GV_THREADS) {
+        float4 v[SB], gn[SB];
+        float ri[SB];
+        float* dst[SB];
+#pragma unroll
+        for (int u = 0; u < SB; ++u) {
+            const int t = t0 + u * GV_THREADS;
+            dst[u] = nullptr;
+            ri[u] = 0.f;
+            if (t < nitems) {
+                int i = 0;
+                while (i + 1 < nxs && L.xs[i + 1].item0 <= t) ++i;
+                const GvXSrc& x = L.xs[i];
+                const int K4 = x.K >> 2, r = t - x.item0, m = r / K4, k = (r - m * K4) * 4;
+                const size_t g = (size_t)(m * x.row_stride + x.row_off) * x.ld + k;
+                v[u] = *reinterpret_cast<const float4*>(x.src + g);
                 if (x.add) {
-                    const float4 a = *reinterpret_cast<const float4*>(x.add + r);
-                    v.x += a.x; v.y += a.y; v.z += a.z; v.w += a.w;
+                    const float4 a = *reinterpret_cast<const float4*>(x.add + g);
+                    v[u].x += a.x; v[u].y += a.y; v[u].z += a.z; v[u].w += a.w;
                 }
-                const float ri = xs_rinv[i * M + m];
-                const T* g = (const T*)x.gain + k;
-                v.x = v.x * ri * to_f32(g[0]);
-                v.y = v.y * ri * to_f32(g[1]);
-                v.z = v.z * ri * to_f32(g[2]);
-                v.w = v.w * ri * to_f32(g[3]);
+                if (x.kind == XS_NORM) {
+                    const T* gp = (const T*)x.gain + k;
+                    gn[u] = make_float4(to_f32(gp[0]), to_f32(gp[1]), to_f32(gp[2]), to_f32(gp[3]));
+                    ri[u] = x.rinv[m];
+                }
+                dst[u] = xsm + x.smem_off + (size_t)m * x.K + k;
             }
-            *reinterpret_cast<float4*>(dst + (size_t)m * x.K + k) = v;
+        }
+#pragma unroll
+        for (int u = 0; u < SB; ++u) {
+            if (!dst[u]) continue;
+            float4 y = v[u];
+            if (ri[u] != 0.f) {
+                y.x = y.x * ri[u] * gn[u].x;
+                y.y = y.y * ri[u] * gn[u].y;
+                y.z = y.z * ri[u] * gn[u].z;
+                y.w = y.w * ri[u] * gn[u].w;
+            }
+            *reinterpret_cast<float4*>(dst[u]) = y;
         }
     }
     __syncthreads();
@@ -282,17 +333,14 @@ gv_kernel(const GvLaunch* __restrict__ L, float* __restrict__ scratch, int* __re
         for (int m = 0; m < M; ++m) acc[r][m] = 0.f;
     float vset[2] = {0.f, 0.f};  // reduced sums of finished accumulator sets (lane-distributed)
     int cur_set = -1;
+    int tile_first = s_begin - ((s_begin - L.ops[cur.op].stage0) % L.ops[cur.op].spt);
 
-    GvWalk w;
-    w.seek(L, s_begin);
-    int tile_first = s_begin - ((s_begin - L->ops[w.op].stage0) % L->ops[w.op].spt);
-    int s = s_begin;
-    while (s < s_end) {
-        // one run: consecutive column chunks of a single segment
-        const int cur_op = w.op, cur_tile = w.tile;
-        const GvOp& o = L->ops[cur_op];
-        const GvSeg& sg = o.seg[w.seg];
-        const int run = min(s_end - s, sg.nck - w.kc);
+    while (have) {
+        const bool have_n = next_batch(nxt);
+        if (have_n) load(nxt, wn);  // in flight while this chunk is multiplied
+
+        const GvOp& o = L.ops[cur.op];
+        const GvSeg& sg = L.segs[o.seg0 + cur.seg];
         if (sg.set != cur_set) {
             if (cur_set >= 0) {
                 float t[NV];
@@ -305,106 +353,92 @@ gv_kernel(const GvLaunch* __restrict__ L, float* __restrict__ scratch, int* __re
             cur_set = sg.set;
         }
         {
-            const int K = sg.K;
-            const T* wr[GV_R];
-#pragma unroll
-            for (int r = 0; r < GV_R; ++r)  // rows past N read the last row; their sums are dropped
-                wr[r] = (const T*)sg.W + (size_t)min(cur_tile * GV_RT + warp * GV_R + r, o.N - 1) * K + lane * EPV;
-            const float* xb = xs_base[sg.xs] + lane * EPV;
-            const int xst = xs_stride[sg.xs];
-            int kc = w.kc;
-            const int kc_end = kc + run;
-            const int kc_full = min(kc_end, K / SC);  // chunks lying wholly inside K
-            for (; kc + U <= kc_full; kc += U) {
-                uint4 wv[U][GV_R];
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-#pragma unroll
-                    for (int r = 0; r < GV_R; ++r) wv[u][r] = ld_stream16(wr[r] + (size_t)(kc + u) * SC);
-#pragma unroll
-                for (int u = 0; u < U; ++u) gv_fma<T, M>(wv[u], xb + (size_t)(kc + u) * SC, xst, acc);
-            }
-            for (; kc < kc_full; ++kc) {
-                uint4 wv[GV_R];
-#pragma unroll
-                for (int r = 0; r < GV_R; ++r) wv[r] = ld_stream16(wr[r] + (size_t)kc * SC);
-                gv_fma<T, M>(wv, xb + (size_t)kc * SC, xst, acc);
-            }
-            if (kc < kc_end && kc * SC + lane * EPV < K) {  // ragged last chunk of the segment
-                uint4 wv[GV_R];
-#pragma unroll
-                for (int r = 0; r < GV_R; ++r) wv[r] = ld_stream16(wr[r] + (size_t)kc * SC);
-                gv_fma<T, M>(wv, xb + (size_t)kc * SC, xst, acc);
-            }
+            const int k = cur.kc * SC + lane * EPV;
+            if (k < sg.K) gv_fma<T, M>(wc, xs_base[sg.xs] + k, xs_stride[sg.xs], acc);
         }
-        const bool tile_end = w.advance(run);
-        s += run;
-        if (!(tile_end || s == s_end)) continue;
-
-        // ------------ finish the tile (or this CTA's part of it)
-        {
-            float t[NV];
+        if (cur.tile_end || cur.range_end) {
+            // ------------ finish the tile (or this CTA's part of it)
+            {
+                float t[NV];
 #pragma unroll
-            for (int r = 0; r < GV_R; ++r)
+                for (int r = 0; r < GV_R; ++r)
 #pragma unroll
-                for (int m = 0; m < M; ++m) { t[r * M + m] = acc[r][m]; acc[r][m] = 0.f; }
-            vset[cur_set] += warp_reduce_scatter<NV>(t, lane);
-        }
-        float v0 = vset[0], v1 = vset[1];
-        vset[0] = vset[1] = 0.f;
-        cur_set = -1;
-        const bool two = o.epi == GEPI_SWIGLU;
-        const int tile_last = tile_first + o.spt - 1;
-        const bool complete = tile_first >= s_begin && tile_last < s_end;
-        const int gtile = o.tile0 + cur_tile;
-        bool do_epi = complete;
-        if (!complete) {
-            const int sid = s_begin >= tile_first ? 0 : 1;
-            float* part = scratch + ((size_t)(blockIdx.x * 2 + sid) * 2) * GV_THREADS + tid;
-            part[0] = v0;
-            if (two) part[GV_THREADS] = v1;
-            __threadfence();
-            __syncthreads();
-            const int c_first = tile_first / Q, c_last = tile_last / Q;
-            if (tid == 0) s_last = atomicAdd(counters + gtile, 1) == c_last - c_first;
-            __syncthreads();
-            if (s_last) {
+                    for (int m = 0; m < M; ++m) { t[r * M + m] = acc[r][m]; acc[r][m] = 0.f; }
+                vset[cur_set] += warp_reduce_scatter<NV>(t, lane);
+            }
+            float v0 = vset[0], v1 = vset[1];
+            vset[0] = vset[1] = 0.f;
+            cur_set = -1;
+            const bool two = o.epi == GEPI_SWIGLU;
+            const int tile_last = tile_first + o.spt - 1;
+            const bool complete = tile_first >= s_begin && tile_last < s_end;
+            const int gtile = o.tile0 + cur.tile;
+            bool do_epi = complete;
+            if (!complete) {
+                const int sid = s_begin >= tile_first ? 0 : 1;
+                float* part = scratch + ((size_t)(blockIdx.x * 2 + sid) * 2) * GV_THREADS + tid;
+                part[0] = v0;
+                if (two) part[GV_THREADS] = v1;
                 __threadfence();
-                v0 = 0.f; v1 = 0.f;
-                for (int cc = c_first; cc <= c_last; ++cc) {
-                    const int sd = cc * Q >= tile_first ? 0 : 1;
-                    const float* pp = scratch + ((size_t)(cc * 2 + sd) * 2) * GV_THREADS + tid;
-                    v0 += __ldcg(pp);
-                    if (two) v1 += __ldcg(pp + GV_THREADS);
+                __syncthreads();
+                const int c_first = tile_first / Q, c_last = tile_last / Q;
+                if (tid == 0) s_last = atomicAdd(counters + gtile, 1) == c_last - c_first;
+                __syncthreads();
+                if (s_last) {
+                    __threadfence();
+                    v0 = 0.f; v1 = 0.f;
+                    for (int cc = c_first; cc <= c_last; ++cc) {
+                        const int sd = cc * Q >= tile_first ? 0 : 1;
+                        const float* pp = scratch + ((size_t)(cc * 2 + sd) * 2) * GV_THREADS + tid;
+                        v0 += __ldcg(pp);
+                        if (two) v1 += __ldcg(pp + GV_THREADS);
+                    }
+                    if (tid == 0) counters[gtile] = 0;
+                    do_epi = true;
                 }
-                if (tid == 0) counters[gtile] = 0;
-                do_epi = true;
+                // every thread has read s_last before a later tile changes it
+                __syncthreads();
             }
-            // every thread has read s_last before a later tile changes it
-            __syncthreads();
-        }
-        if (do_epi && lane < NV) {
-            const int r = lane / M, m = lane % M;
-            const int n = cur_tile * GV_RT + warp * GV_R + r;
-            if (n < o.N) {
-                float* y = o.y + (size_t)m * o.ldy + n;
-                switch (o.epi) {
-                    case GEPI_STORE: *y = v0; break;
-                    case GEPI_ACC: *y += v0; break;
-                    case GEPI_ACC_ADD: *y += v0 + o.add[(size_t)m * o.ldy + n]; break;
-                    default: *y = silu_f(v0) * v1; break;
+            if (do_epi && lane < NV) {
+                const int r = lane / M, m = lane % M;
+                const int n = cur.tile * GV_RT + warp * GV_R + r;
+                if (n < o.N) {
+                    float* y = o.y + (size_t)m * o.ldy + n;
+                    switch (o.epi) {
+                        case GEPI_STORE: *y = v0; break;
+                        case GEPI_ACC: *y += v0; break;
+                        case GEPI_ACC_ADD: *y += v0 + o.add[(size_t)m * o.ldy + n]; break;
+                        default: *y = silu_f(v0) * v1; break;
+                    }
                 }
             }
+            tile_first = tile_last + 1;
         }
-        tile_first = tile_last + 1;
+        cur = nxt;
+#pragma unroll
+        for (int r = 0; r < GV_R; ++r) wc[r] = wn[r];
+        have = have_n;
+    }
+
+    // ------------ post-norm (1/rms of the next pass's input rows) by the last
+    // CTA to finish
+    if (L.post.rows > 0) {
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) s_last = atomicAdd(done, 1) == (int)gridDim.x - 1;
+        __syncthreads();
+        if (s_last) {
+            __threadfence();
+            post_rinv(L.post);
+            if (tid == 0) *done = 0;
+        }
     }
 }
 
 // ------------------------------------------------------------ SIMT GEMM
 // The same launch descriptor for many rows (prompt prefill): 64x64 output
-// tiles, float32 FMA.  Every x source must be RAW (normalised inputs are
-// produced beforehand).  grid.x = 64-row tiles over all ops, grid.y = 64-row
-// blocks of the M input rows.
+// tiles, float32 FMA.  grid.x = 64-row tiles over all ops, grid.y = 64-row
+// blocks of the M input rows.  Every source is read from global memory.
 constexpr int GB = 64, GK = 32;
 template <typename T>
 __global__ void __launch_bounds__(256) gemm_kernel(const GvLaunch* __restrict__ L) {
@@ -425,7 +459,7 @@ __global__ void __launch_bounds__(256) gemm_kernel(const GvLaunch* __restrict__ 
 #pragma unroll
             for (int jx = 0; jx < 4; ++jx) acc[u][i][jx] = 0.f;
     for (int s = 0; s < op.nseg; ++s) {
-        const GvSeg sg = op.seg[s];
+        const GvSeg sg = L->segs[op.seg0 + s];
         const GvXSrc& xd = L->xs[sg.xs];
         const float* X = xd.src + (size_t)xd.row_off * xd.ld;
         const size_t xst = (size_t)xd.row_stride * xd.ld;

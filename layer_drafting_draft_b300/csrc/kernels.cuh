@@ -34,7 +34,8 @@ __global__ void prep_embed_kernel(int kind, int step, int gamma, int M,
                                   int max_seq, const int* __restrict__ dtok, int gmax,
                                   int* row_pos, int* row_seq, int* row_tok, int* row_base,
                                   const T* __restrict__ E, float* __restrict__ h, int d, int V,
-                                  int* status) {
+                                  int* status, GvPost post) {
+    __shared__ float red[32];
     grid_dep_wait();
     const int m = blockIdx.x;
     if (m >= M) return;
@@ -66,7 +67,18 @@ __global__ void prep_embed_kernel(int kind, int step, int gamma, int M,
         row_pos[m] = pos; row_seq[m] = b; row_tok[m] = tok; row_base[m] = base;
     }
     const T* e = E + (size_t)tok * d;
-    for (int i = threadIdx.x; i < d; i += blockDim.x) h[(size_t)m * d + i] = to_f32(e[i]);
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < d; i += blockDim.x) {
+        const float v = to_f32(e[i]);
+        h[(size_t)m * d + i] = v;
+        ss += v * v;
+    }
+    // 1/rms of the embedded rows for the first weight pass (rows map one to
+    // one here)
+    if (post.rows > 0) {
+        ss = block_sum(ss, red);
+        if (threadIdx.x == 0) post.rinv[m] = 1.0f / sqrtf(ss / (float)d + post.eps);
+    }
 }
 
 // -------------------------------------------------------------------- RMSNorm
@@ -138,121 +150,6 @@ ES_DEV int block_sample_q40(F weight, int V, uint64_t u, uint64_t* sh /* >= 34 *
     }
     __syncthreads();
     return (int)sh[33];
-}
-
-// Argmax over float32 values, lowest index on ties (block-wide).
-template <typename F>
-ES_DEV int block_argmax(F val, int V, float* shv, int* shi) {
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int i = tid; i < V; i += blockDim.x) {
-        const float v = val(i);
-        if (v > bv || (v == bv && i < bi)) { bv = v; bi = i; }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-    }
-    __syncthreads();
-    if (lane == 0) { shv[wid] = bv; shi[wid] = bi; }
-    __syncthreads();
-    if (wid == 0) {
-        bv = lane < (int)(blockDim.x >> 5) ? shv[lane] : -INFINITY;
-        bi = lane < (int)(blockDim.x >> 5) ? shi[lane] : 0x7fffffff;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-        }
-        if (lane == 0) shi[0] = bi;
-    }
-    __syncthreads();
-    const int r = shi[0];
-    __syncthreads();
-    return r;
-}
-
-// -------------------------------------------------------------------- accept / resample
-// One block per sequence.  p [B][gamma+1][V], q [B][gamma][V] (probabilities,
-// or logits when greedy), d [B][gmax].  Draws: u_explicit [B][gamma+1] when
-// given, else the phase's slots gamma..2gamma.  Commits tokens when `tokens`
-// is set (tokens[b][n_b + t], n_b += n_acc + 1, phase[b] += 1).
-struct AcceptArgs {
-    const float* p; const float* q; const int* d; int gmax; int gamma, V, greedy;
-    const uint64_t* u_explicit; const RunParams* prm; int64_t* phase;
-    int* n_acc; int* out_tok;  // out_tok [B][gamma+1]
-    int* tokens; int max_seq; int* n_commit;
-    const int* n_limit;  // a sequence with n_commit >= n_limit is finished: no commit
-};
-__global__ void __launch_bounds__(1024) accept_kernel(AcceptArgs a) {
-    __shared__ float red[32];
-    __shared__ int redi[32];
-    __shared__ uint64_t sh[34];
-    __shared__ int s_j;
-    grid_dep_wait();
-    const int b = blockIdx.x, g = a.gamma, V = a.V;
-    const float* P = a.p + (size_t)b * (g + 1) * V;
-    const float* Q = a.q + (size_t)b * g * V;
-    const int* d = a.d + b * a.gmax;
-    // greedy < 0: decided by the run's temperature (0 = greedy)
-    const int greedy = a.greedy >= 0 ? a.greedy : (a.prm->temperature == 0.f ? 1 : 0);
-    uint64_t seed = 0;
-    int64_t ph = 0;
-    // greedy decisions consume no draws: the run parameters and phase counter
-    // are read only for sampled runs without caller-given draws
-    if (!greedy && !a.u_explicit) { seed = a.prm->seed; ph = a.phase[b]; }
-    auto draw = [&](int t) -> uint64_t {  // t = 0..gamma (accept tests, then residual)
-        return a.u_explicit ? a.u_explicit[(size_t)b * (g + 1) + t] : es_draw(seed, b, ph, g + t, g);
-    };
-    int j = g;
-    if (greedy) {
-        for (int i = 0; i < g; ++i) {
-            const float* Pi = P + (size_t)i * V;
-            const int am = block_argmax([&](int v) { return Pi[v]; }, V, red, redi);
-            if (am != d[i]) { j = i; break; }
-        }
-    } else if (threadIdx.x == 0) {
-        for (int i = 0; i < g; ++i) {
-            const int x = d[i];
-            if (x < 0 || x >= V) { j = i; break; }  // not a token: rejected
-            const float u = uniform24(draw(i));
-            if (!(__fmul_rn(u, Q[(size_t)i * V + x]) < P[(size_t)i * V + x])) { j = i; break; }
-        }
-        s_j = j;
-    }
-    if (!greedy) { __syncthreads(); j = s_j; }
-    const float* Pj = P + (size_t)j * V;
-    int y;
-    if (greedy) {
-        y = block_argmax([&](int v) { return Pj[v]; }, V, red, redi);
-    } else {
-        const uint64_t u = draw(g);
-        if (j < g) {
-            const float* Qj = Q + (size_t)j * V;
-            y = block_sample_q40([&](int v) { return fmaxf(0.f, __fsub_rn(Pj[v], Qj[v])); }, V, u, sh);
-            if (y < 0) y = block_sample_q40([&](int v) { return Pj[v]; }, V, u, sh);
-        } else {
-            y = block_sample_q40([&](int v) { return Pj[v]; }, V, u, sh);
-        }
-        if (y < 0) y = 0;
-    }
-    if (threadIdx.x == 0) {
-        a.n_acc[b] = j;
-        int* ot = a.out_tok + (size_t)b * (g + 1);
-        for (int t = 0; t <= g; ++t) ot[t] = t < j ? d[t] : (t == j ? y : -1);
-        if (a.tokens && a.n_commit[b] < a.n_limit[b]) {
-            const int n = a.n_commit[b];
-            int* tk = a.tokens + (size_t)b * a.max_seq;
-            for (int t = 0; t < j && n + t < a.max_seq; ++t) tk[n + t] = d[t];
-            if (n + j < a.max_seq) tk[n + j] = y;
-            a.n_commit[b] = n + j + 1;
-            a.phase[b] += 1;
-        }
-    }
 }
 
 // Sampling hook: row b of unnormalised weights w [B][V] with draw u[b].

@@ -29,6 +29,7 @@ struct SampleArgs {
     const float* z; float* p; int V, nb, chunk;
     int per_seq, off, ld_rows;
     const RunParams* prm; const int64_t* phase; int gamma;
+    int greedy;                // 1 / 0, or -1: greedy when prm->temperature == 0
     int* dtok; int gmax;       // draw d[b][i] when set
     float* part;               // [rows][nb][2]
     unsigned long long* mass;  // [rows][nb]
@@ -80,6 +81,52 @@ ES_DEV int block_find_q40(F weight, int n, uint64_t t, uint64_t* sh) {
     return (int)sh[33];
 }
 
+// Block-wide inclusive prefix sum of one u64 per thread (blockDim.x a
+// multiple of 32, <= 1024); sh >= 33 entries.  Also returns the total.
+ES_DEV uint64_t block_incl_scan_u64(uint64_t v, uint64_t* sh, uint64_t* total) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
+    const uint64_t incl = warp_incl_scan_u64(v, lane);
+    __syncthreads();
+    if (lane == 31) sh[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        const uint64_t w = lane < nw ? sh[lane] : 0;
+        const uint64_t wi = warp_incl_scan_u64(w, lane);
+        sh[lane] = wi - w;
+        if (lane == 31) sh[32] = wi;
+    }
+    __syncthreads();
+    const uint64_t r = sh[wid] + incl;
+    *total = sh[32];
+    __syncthreads();
+    return r;
+}
+
+// The chunk of a categorical draw from per-chunk integer masses (nb <=
+// blockDim.x, read with __ldcg at stride `stride`): t = floor(u * total /
+// 2^64), the chunk whose prefix range holds t and t relative to its start.
+// Returns the total (0: no chunk).  Whole block.
+ES_DEV uint64_t block_locate_chunk(const unsigned long long* mass, int stride, int nb, uint64_t u,
+                                   int* chunk, uint64_t* t_rel, uint64_t* sh) {
+    __shared__ int s_ck;
+    __shared__ uint64_t s_tr;
+    const int tid = threadIdx.x;
+    const uint64_t w = tid < nb ? (uint64_t)__ldcg(mass + (size_t)tid * stride) : 0;
+    uint64_t total;
+    const uint64_t incl = block_incl_scan_u64(w, sh, &total);
+    if (tid == 0) { s_ck = -1; s_tr = 0; }
+    __syncthreads();
+    if (total > 0) {
+        const uint64_t t = __umul64hi(u, total);
+        if (w > 0 && incl - w <= t && t < incl) { s_ck = tid; s_tr = t - (incl - w); }
+    }
+    __syncthreads();
+    *chunk = s_ck;
+    *t_rel = s_tr;
+    __syncthreads();
+    return total;
+}
+
 ES_DEV bool better(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
 
 __global__ void __launch_bounds__(SM_THREADS) softmax_part_kernel(SampleArgs a) {
@@ -90,10 +137,10 @@ __global__ void __launch_bounds__(SM_THREADS) softmax_part_kernel(SampleArgs a) 
     const int r = blockIdx.x, c = blockIdx.y, b = r / a.per_seq, i = r % a.per_seq + a.off;
     const float* z = a.z + ((size_t)b * a.ld_rows + i) * a.V;
     const int v0 = c * a.chunk, v1 = min(a.V, v0 + a.chunk);
-    const float T = a.prm->temperature;
+    const float T = a.greedy > 0 ? 0.f : a.prm->temperature;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     float* out = a.part + ((size_t)r * a.nb + c) * 2;
-    if (T == 0.f) {
+    if (a.greedy > 0 || (a.greedy < 0 && T == 0.f)) {
         float bv = -INFINITY;
         int bi = 0x7fffffff;
         for (int v = v0 + tid; v < v1; v += SM_THREADS)
@@ -148,10 +195,10 @@ __global__ void __launch_bounds__(SM_THREADS) softmax_finish_kernel(SampleArgs a
     const float* z = a.z + row;
     float* p = a.p + row;
     const int v0 = c * a.chunk, v1 = min(a.V, v0 + a.chunk);
-    const float T = a.prm->temperature;
+    const float T = a.greedy > 0 ? 0.f : a.prm->temperature;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const float* part = a.part + (size_t)r * a.nb * 2;
-    if (T == 0.f) {
+    if (a.greedy > 0 || (a.greedy < 0 && T == 0.f)) {
         // greedy: the logits themselves are kept; the draw is the argmax
         for (int v = v0 + tid; v < v1; v += SM_THREADS) p[v] = z[v];
         if (a.dtok && c == 0 && tid == 0) {
@@ -202,37 +249,169 @@ __global__ void __launch_bounds__(SM_THREADS) softmax_finish_kernel(SampleArgs a
     if (!s_last) return;
     __threadfence();
     // last chunk CTA of the row: locate the draw
-    __shared__ int s_chunk;
-    __shared__ unsigned long long s_t;
-    if (tid == 0) {
-        const unsigned long long* mr = a.mass + (size_t)r * a.nb;
-        unsigned long long total = 0;
-        for (int k = 0; k < a.nb; ++k) total += __ldcg(mr + k);
-        int ck = -1;
-        unsigned long long tt = 0;
-        if (total > 0) {
-            const uint64_t u = es_draw(a.prm->seed, b, a.phase[b], i, a.gamma);
-            const unsigned long long t = __umul64hi(u, total);
-            unsigned long long pre = 0;
-            for (int k = 0; k < a.nb; ++k) {
-                const unsigned long long w = __ldcg(mr + k);
-                if (t < pre + w) { ck = k; tt = t - pre; break; }
-                pre += w;
-            }
-        }
-        s_chunk = ck;
-        s_t = tt;
-        a.counters[r] = 0;
-    }
-    __syncthreads();
-    const int ck = s_chunk;
+    if (tid == 0) a.counters[r] = 0;
+    const uint64_t u = es_draw(a.prm->seed, b, a.phase[b], i, a.gamma);
+    int ck;
+    uint64_t t_rel;
+    block_locate_chunk(a.mass + (size_t)r * a.nb, 1, a.nb, u, &ck, &t_rel, sh);
     if (ck < 0) {
         if (tid == 0) a.dtok[b * a.gmax + i] = 0;
         return;
     }
     const int c0 = ck * a.chunk, c1 = min(a.V, c0 + a.chunk);
-    const int idx = block_find_q40([&](int k) { return __ldcg(p + c0 + k); }, c1 - c0, s_t, sh);
+    const int idx = block_find_q40([&](int k) { return __ldcg(p + c0 + k); }, c1 - c0, t_rel, sh);
     if (tid == 0) a.dtok[b * a.gmax + i] = c0 + idx;
+}
+
+// ------------------------------------------------------------ accept / resample
+// Grid (B, nb), one CTA per vocabulary chunk of each sequence.  p [B][g+1][V]
+// and q [B][g][V] are probabilities (greedy: logits), d [B][gmax] the draft
+// tokens.  Every CTA finds the first rejected slot j (sampled: the accept
+// test fl(u * q_i(d_i)) < p_i(d_i) with the draw of slot g+i; greedy:
+// d_i == argmax p_i, from the per-chunk argmax partials `gpart` of the g+1
+// p rows).  Sampled runs then draw y from max(0, p_j - q_j) (j < g; from p_j
+// when that has no integer mass) or from p_g (every draft accepted): each
+// CTA adds the integer masses of its chunk, the last one locates the draw.
+// The deciding CTA writes n_acc and the tokens and, when `tokens` is set,
+// commits them (n_commit += j + 1 unless the sequence reached n_limit;
+// phase += 1).
+struct AcceptArgs {
+    const float* p; const float* q; const int* d; int gmax, gamma, V, nb, chunk;
+    int greedy;                    // 1 / 0, or -1: greedy when prm->temperature == 0
+    const uint64_t* u_explicit;    // [B][g+1] draws, or null: the phase's slots g..2g
+    const RunParams* prm; int64_t* phase;
+    const float* gpart;            // [B*(g+1)][nb][2] (greedy)
+    unsigned long long* mass;      // [B][nb][2]
+    int* counters;                 // [B]
+    int* n_acc; int* out_tok;      // [B], [B][g+1] (-1 past n_acc+1)
+    int* tokens; int max_seq; int* n_commit; const int* n_limit;
+};
+
+__global__ void __launch_bounds__(SM_THREADS) accept_kernel(AcceptArgs a) {
+    __shared__ int s_j, s_y, s_last;
+    __shared__ int s_am[17];
+    __shared__ uint64_t sh[34];
+    __shared__ unsigned long long rs[2][SM_THREADS / 32];
+    grid_dep_wait();
+    const int b = blockIdx.x, c = blockIdx.y, g = a.gamma, V = a.V;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int greedy = a.greedy >= 0 ? a.greedy : (a.prm->temperature == 0.f ? 1 : 0);
+    const float* P = a.p + (size_t)b * (g + 1) * V;
+    const float* Q = a.q + (size_t)b * g * V;
+    const int* d = a.d + b * a.gmax;
+    if (greedy) {
+        if (c != 0) return;
+        // argmax of each p row from the chunk partials (warp per row)
+        for (int i = wid; i <= g; i += SM_THREADS / 32) {
+            const float* gp = a.gpart + ((size_t)b * (g + 1) + i) * a.nb * 2;
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
+            for (int k = lane; k < a.nb; k += 32) {
+                const float v = gp[2 * k];
+                const int vi = __float_as_int(gp[2 * k + 1]);
+                if (better(v, vi, bv, bi)) { bv = v; bi = vi; }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+            }
+            if (lane == 0) s_am[i] = bi;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            int j = g;
+            for (int i = 0; i < g; ++i)
+                if (s_am[i] != d[i]) { j = i; break; }
+            s_j = j;
+            s_y = s_am[j];
+        }
+    } else {
+        uint64_t seed = 0;
+        int64_t ph = 0;
+        if (!a.u_explicit) { seed = a.prm->seed; ph = a.phase[b]; }
+        auto draw = [&](int t) -> uint64_t {  // t = 0..g (accept tests, then the residual)
+            return a.u_explicit ? a.u_explicit[(size_t)b * (g + 1) + t] : es_draw(seed, b, ph, g + t, g);
+        };
+        if (tid == 0) {
+            int j = g;
+            for (int i = 0; i < g; ++i) {
+                const int x = d[i];
+                if (x < 0 || x >= V) { j = i; break; }  // not a token: rejected
+                const float u = uniform24(draw(i));
+                if (!(__fmul_rn(u, Q[(size_t)i * V + x]) < P[(size_t)i * V + x])) { j = i; break; }
+            }
+            s_j = j;
+        }
+        __syncthreads();
+        const int j = s_j;
+        const float* Pj = P + (size_t)j * V;
+        const float* Qj = Q + (size_t)j * V;
+        const int v0 = c * a.chunk, v1 = min(V, v0 + a.chunk);
+        unsigned long long mr = 0, mp = 0;
+        for (int v = v0 + tid; v < v1; v += SM_THREADS) {
+            const float pv = Pj[v];
+            mp += q40(pv);
+            mr += j < g ? q40(fmaxf(0.f, __fsub_rn(pv, Qj[v]))) : q40(pv);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            mr += __shfl_xor_sync(0xffffffffu, mr, o);
+            mp += __shfl_xor_sync(0xffffffffu, mp, o);
+        }
+        if (lane == 0) { rs[0][wid] = mr; rs[1][wid] = mp; }
+        __syncthreads();
+        if (tid == 0) {
+            unsigned long long t0 = 0, t1 = 0;
+            for (int w = 0; w < SM_THREADS / 32; ++w) { t0 += rs[0][w]; t1 += rs[1][w]; }
+            unsigned long long* ms = a.mass + ((size_t)b * a.nb + c) * 2;
+            ms[0] = t0;
+            ms[1] = t1;
+            __threadfence();
+            s_last = atomicAdd(a.counters + b, 1) == a.nb - 1;
+        }
+        __syncthreads();
+        if (!s_last) return;
+        __threadfence();
+        if (tid == 0) a.counters[b] = 0;
+        const uint64_t u = draw(g);
+        int ck;
+        uint64_t t_rel;
+        // the residual; with no integer mass left, the base distribution p_j
+        int use_p = 0;
+        if (block_locate_chunk(a.mass + (size_t)b * a.nb * 2, 2, a.nb, u, &ck, &t_rel, sh) == 0) {
+            use_p = 1;
+            block_locate_chunk(a.mass + (size_t)b * a.nb * 2 + 1, 2, a.nb, u, &ck, &t_rel, sh);
+        }
+        int y = 0;
+        if (ck >= 0) {
+            const int c0 = ck * a.chunk, c1 = min(V, c0 + a.chunk);
+            const bool resid = j < g && !use_p;
+            y = c0 + block_find_q40(
+                         [&](int k) {
+                             const float pv = Pj[c0 + k];
+                             return resid ? fmaxf(0.f, __fsub_rn(pv, Qj[c0 + k])) : pv;
+                         },
+                         c1 - c0, t_rel, sh);
+        }
+        if (tid == 0) s_y = y;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const int j = s_j, y = s_y;
+        a.n_acc[b] = j;
+        int* ot = a.out_tok + (size_t)b * (g + 1);
+        for (int t = 0; t <= g; ++t) ot[t] = t < j ? d[t] : (t == j ? y : -1);
+        if (a.tokens && a.n_commit[b] < a.n_limit[b]) {
+            const int n = a.n_commit[b];
+            int* tk = a.tokens + (size_t)b * a.max_seq;
+            for (int t = 0; t < j && n + t < a.max_seq; ++t) tk[n + t] = d[t];
+            if (n + j < a.max_seq) tk[n + j] = y;
+            a.n_commit[b] = n + j + 1;
+            a.phase[b] += 1;
+        }
+    }
 }
 
 }  // namespace es
