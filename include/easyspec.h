@@ -108,6 +108,7 @@ typedef struct {
     void *cuda_stream;        /* cudaStream_t, or NULL for the default stream */
 } es_config;
 
+
 /* Per-run counters filled by generate() (may be NULL). */
 typedef struct {
     int64_t phases;           /* drafting-and-verification iterations run     */

@@ -18,6 +18,7 @@
 // merges them in split order and writes the head outputs.
 #pragma once
 #include "common.cuh"
+#include "gemv.cuh"
 
 namespace es {
 
@@ -47,6 +48,8 @@ struct AttnArgs {
     float* part;   // [M][nl][H][nsplit][hd + 2]
     int* counters; // [M][nl][Hkv]
     const int* row_pos; const int* row_seq; const int* row_base;
+    const GvLaunch* next;  // the weight pass that follows (its weights are requested into L2), or null
+    int next_bf16;
 };
 
 // dynamic shared memory (floats): qs G*(hd+4) | ks 64*(hd+4) | vs 64*(hd+4) |
@@ -55,19 +58,26 @@ inline size_t attn_smem_bytes(int G, int hd, int nsplit) {
     return sizeof(float) * ((size_t)G * (hd + 4) + 2 * 64 * (hd + 4) + (size_t)G * (nsplit > 64 ? nsplit : 64));
 }
 
+// A cache element read through L2 (entries are written by other CTAs).
+ES_DEV float ldcg_f(const float* p) { return __ldcg(p); }
+ES_DEV float ldcg_f(const bf16* p) {
+    return __uint_as_float((uint32_t)__ldcg(reinterpret_cast<const unsigned short*>(p)) << 16);
+}
+
+// One work item: row m, layer slot x kv head `jy`, position split `sp`.
+// Whole CTA (ATT_THREADS threads).
 template <typename T>
-__global__ void __launch_bounds__(ATT_THREADS) attn_kernel(AttnArgs a) {
+ES_DEV void attn_item(const AttnArgs& a, int m, int jy, int sp) {
     extern __shared__ __align__(16) float asm_[];
     __shared__ int s_last;
-    grid_dep_wait();
-    grid_dep_launch();
     const int Hkv = a.g.Hkv, hd = a.g.hd, half = hd / 2, G = a.H / Hkv, ld = hd + 4;
-    const int m = blockIdx.x, j = blockIdx.y / Hkv, hk = blockIdx.y % Hkv, sp = blockIdx.z;
-    const int pos = a.row_pos[m];
+    const int j = jy / Hkv, hk = jy % Hkv;
+    const int pos = __ldcg(a.row_pos + m);
     const int p0 = sp * PAGE;
     if (pos < 0 || p0 > pos) return;
+    __syncthreads();  // the previous item of this CTA is done with shared memory
     const int n = min(PAGE, pos + 1 - p0);
-    const int rb = a.row_base[m], bpos = a.row_pos[rb], seq = a.row_seq[m];
+    const int rb = __ldcg(a.row_base + m), bpos = __ldcg(a.row_pos + rb), seq = __ldcg(a.row_seq + m);
     const int tid = threadIdx.x, layer = a.layer[j];
     float* qs = asm_;
     float* ks = qs + G * ld;
@@ -93,8 +103,8 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_kernel(AttnArgs a) {
             for (int u = 0; u < VPT; ++u) {
                 const int t = base + u * ATT_THREADS + tid;
                 if (t < nv) {
-                    kv4[u] = *reinterpret_cast<const uint4*>(Kp + (size_t)t * EPV);
-                    vv4[u] = *reinterpret_cast<const uint4*>(Vp + (size_t)t * EPV);
+                    kv4[u] = __ldcg(reinterpret_cast<const uint4*>(Kp + (size_t)t * EPV));
+                    vv4[u] = __ldcg(reinterpret_cast<const uint4*>(Vp + (size_t)t * EPV));
                 }
             }
         }
@@ -102,7 +112,7 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_kernel(AttnArgs a) {
             for (int t = tid; t < G * half; t += ATT_THREADS) {
                 const int h = t / half, i = t % half;
                 const float c = csq[2 * i], sn = csq[2 * i + 1];
-                const float x0 = q[h * hd + i], x1 = q[h * hd + i + half];
+                const float x0 = __ldcg(q + h * hd + i), x1 = __ldcg(q + h * hd + i + half);
                 qs[h * ld + i] = (x0 * c - x1 * sn) * scale;
                 qs[h * ld + i + half] = (x1 * c + x0 * sn) * scale;
             }
@@ -133,17 +143,17 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_kernel(AttnArgs a) {
             if (p < bpos) {
                 const T* kr = kv_ptr<T>(a.g, seq, p, layer, 0, hk);
                 const T* vr = kv_ptr<T>(a.g, seq, p, layer, 1, hk);
-                k0 = to_f32(kr[e]); k1 = to_f32(kr[e + half]);
-                v0 = to_f32(vr[e]); v1 = to_f32(vr[e + half]);
+                k0 = ldcg_f(kr + e); k1 = ldcg_f(kr + e + half);
+                v0 = ldcg_f(vr + e); v1 = ldcg_f(vr + e + half);
             } else {
                 const size_t r = (size_t)(rb + (p - bpos)) * kvd + (size_t)hk * hd;
                 const float* cs = a.rope + (size_t)p * hd;
                 const float c = cs[2 * e], sn = cs[2 * e + 1];
-                const float x0 = a.k[j][r + e], x1 = a.k[j][r + e + half];
+                const float x0 = __ldcg(a.k[j] + r + e), x1 = __ldcg(a.k[j] + r + e + half);
                 k0 = to_f32(from_f32<T>(x0 * c - x1 * sn));
                 k1 = to_f32(from_f32<T>(x1 * c + x0 * sn));
-                v0 = to_f32(from_f32<T>(a.v[j][r + e]));
-                v1 = to_f32(from_f32<T>(a.v[j][r + e + half]));
+                v0 = to_f32(from_f32<T>(__ldcg(a.v[j] + r + e)));
+                v1 = to_f32(from_f32<T>(__ldcg(a.v[j] + r + e + half)));
             }
             ks[i * ld + e] = k0; ks[i * ld + e + half] = k1;
             vs[i * ld + e] = v0; vs[i * ld + e + half] = v1;
@@ -249,6 +259,23 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_kernel(AttnArgs a) {
         outp[t] = num;
     }
     if (tid == 0) *ctr = 0;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(ATT_THREADS) attn_kernel(AttnArgs a) {
+    grid_dep_wait();
+    grid_dep_launch();
+    // Attention leaves HBM mostly idle: stream this CTA's share of the next
+    // weight pass into L2 first (its weights do not depend on anything).
+    if (a.next) {
+        const int cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+        const int ncta = gridDim.x * gridDim.y * gridDim.z;
+        const int ns = a.next->nstages;
+        const int s0 = (int)((long)ns * cta / ncta), s1 = (int)((long)ns * (cta + 1) / ncta);
+        if (a.next_bf16) gv_prefetch_l2<bf16>(*a.next, s0, s1);
+        else gv_prefetch_l2<float>(*a.next, s0, s1);
+    }
+    attn_item<T>(a, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 
 }  // namespace es

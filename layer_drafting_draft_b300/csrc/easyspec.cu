@@ -50,6 +50,8 @@ struct Rec {
     double bytes = 0;          // algorithmic bytes (weights + activations), 0 if not modelled
     const GvLaunch* gv = nullptr;           // device copy (after upload)
     std::shared_ptr<GvLaunch> host;         // host copy while the plan is built
+    size_t next_gv = 0;                     // attention: index of the weight pass after it
+    bool bf16 = false;                      // weights are bf16
     int grid = 0, smem = 0, M = 0, ntiles64 = 0;
     NormArgs norm{};
     AttnArgs attn{};
@@ -393,6 +395,9 @@ Rec finish_gv(es_ctx* c, GvBuild& b, const char* name) {
 }
 
 void upload_plan(es_ctx* c, Plan& p) {
+    // each attention launch streams in the weights of the pass after it
+    for (size_t i = 0; i + 1 < p.recs.size(); ++i)
+        if (p.recs[i].kind == R_ATTN && p.recs[i + 1].kind == R_GV) p.recs[i].next_gv = i + 1;
     for (Rec& r : p.recs) {
         if (!r.host) continue;
         const size_t bytes = sizeof(GvLaunch);
@@ -403,6 +408,11 @@ void upload_plan(es_ctx* c, Plan& p) {
         r.gv = reinterpret_cast<const GvLaunch*>(c->arena + at);
         r.host.reset();
     }
+    for (Rec& r : p.recs)
+        if (r.next_gv) {
+            r.attn.next = p.recs[r.next_gv].gv;
+            r.attn.next_bf16 = r.bf16 ? 1 : 0;
+        }
 }
 
 NormArgs norm_args(Model& m, float* h, const float* add) {
@@ -437,6 +447,7 @@ Rec attn_rec(es_ctx* c, Model& m, int l0, int n, int M) {
     a.part = m.part; a.counters = c->att_counters;
     a.row_pos = m.row_pos; a.row_seq = m.row_seq; a.row_base = m.row_base;
     r.g3 = dim3(M, n * m.Hkv, m.nsplit);
+    r.bf16 = m.dtype == ES_DTYPE_BF16;
     r.smem = (int)attn_smem_bytes(m.H / m.Hkv, m.hd, m.nsplit);
     if (r.smem > 200 * 1024) arg_fail(ES_ERR_ARG, "attention needs %d bytes of shared memory (max_seq too large)", r.smem);
     r.M = M;
@@ -625,14 +636,23 @@ void run_rec(es_ctx* c, const Rec& r) {
     }
 }
 
+EmbedArgs embed_args(es_ctx* c, Model& m, const Plan& plan, int kind, int step, int gamma, int M) {
+    EmbedArgs e;
+    memset(&e, 0, sizeof e);
+    e.kind = kind; e.step = step; e.gamma = gamma; e.M = M;
+    e.n_commit = c->n_commit; e.tokens = c->tokens; e.max_seq = c->cfg.max_seq; e.dtok = c->dtok;
+    e.gmax = c->cfg.max_gamma; e.row_pos = m.row_pos; e.row_seq = m.row_seq; e.row_tok = m.row_tok;
+    e.row_base = m.row_base; e.E = m.embed; e.h = m.h; e.d = m.d; e.V = m.V; e.status = c->status;
+    e.post = plan.first;
+    return e;
+}
+
 // Embedding of the rows described by `kind` (or by the host), then the
 // planned forward (and its head, if planned).
 template <typename T>
 void run_forward(es_ctx* c, Model& m, const Plan& plan, int kind, int step, int gamma, int M) {
-    launch(c, "prep_embed", 0.0, prep_embed_kernel<T>, dim3(M), dim3(256), (size_t)0, kind, step, gamma, M,
-           (const int*)c->n_commit, (const int*)c->tokens, c->cfg.max_seq, (const int*)c->dtok,
-           c->cfg.max_gamma, m.row_pos, m.row_seq, m.row_tok, m.row_base, (const T*)m.embed, m.h, m.d, m.V,
-           c->status, plan.first);
+    launch(c, "prep_embed", 0.0, prep_embed_kernel<T>, dim3(M), dim3(256), (size_t)0,
+           embed_args(c, m, plan, kind, step, gamma, M));
     for (const Rec& r : plan.recs) run_rec<T>(c, r);
 }
 

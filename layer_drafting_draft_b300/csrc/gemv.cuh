@@ -57,6 +57,7 @@ constexpr int GV_MAX_SEG = 16;                 // segments per op
 constexpr int GV_MAX_OPS = 32;
 constexpr int GV_XSMEM_MAX = 26 * 1024;        // floats of staged activations (104 KB)
 constexpr int GV_CTAS_PER_SM = 2;
+constexpr int GV_U = 1;                        // chunks per load batch (two batches in flight)
 constexpr int GV_SCRATCH_CTAS = 1024;          // partial-sum slots
 constexpr int GV_COUNTERS = 65536;             // arrival counters (tiles per launch)
 constexpr int GV_SCRATCH_FLOATS = GV_SCRATCH_CTAS * 2 * 2 * GV_THREADS;
@@ -181,7 +182,9 @@ ES_DEV void post_rinv(const GvPost& p) {
 }
 
 // ------------------------------------------------------------ kernel
-// acc[r][m] += W-vector(r) . x-vector(m) for one 16-byte column vector.
+// acc[r][m] += W-vector(r) . x-vector(m) for one 16-byte column vector; x in
+// shared memory or in global memory (through L1: all warps of the CTA read
+// the same activation vectors).
 template <typename T, int M>
 ES_DEV void gv_fma(const uint4 (&w)[GV_R], const float* __restrict__ x, int xst, float (&acc)[GV_R][M]) {
     constexpr int EPV = 16 / sizeof(T);
@@ -203,69 +206,124 @@ ES_DEV void gv_fma(const uint4 (&w)[GV_R], const float* __restrict__ x, int xst,
     }
 }
 
-// The CTA's stage range, walked one chunk at a time.
+// The CTA's stage range, walked in batches of up to GV_U chunks of one
+// segment.
 struct GvBatch {
-    int op, tile, seg, kc;
-    bool tile_end;   // the chunk completes its tile
-    bool range_end;  // the chunk is the last of this CTA's range
+    int op, tile, seg, kc, n;
+    bool tile_end;   // the batch completes its tile
+    bool range_end;  // the batch is the last of this CTA's range
 };
 
+// Copy a launch descriptor into shared memory (whole CTA; synchronises).
+ES_DEV void gv_load_desc(GvLaunch& L, const GvLaunch* __restrict__ Lg) {
+    const int4* src = reinterpret_cast<const int4*>(Lg);
+    int4* dst = reinterpret_cast<int4*>(&L);
+    for (int i = threadIdx.x; i < (int)(sizeof(GvLaunch) / 16); i += blockDim.x) dst[i] = src[i];
+    __syncthreads();
+}
+
+// The 16-byte weight vectors of batch b for this thread's 4 rows.
+template <typename T>
+ES_DEV void gv_load_batch(const GvLaunch& L, const GvBatch& b, uint4 (&wv)[GV_U][GV_R]) {
+    constexpr int EPV = 16 / sizeof(T);
+    constexpr int SC = GV_ROW_BYTES / sizeof(T);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const GvOp& o = L.ops[b.op];
+    const GvSeg& sg = L.segs[o.seg0 + b.seg];
+#pragma unroll
+    for (int r = 0; r < GV_R; ++r) {
+        // rows past N read the last row; their sums are dropped
+        const T* wr = (const T*)sg.W + (size_t)min(b.tile * GV_RT + warp * GV_R + r, o.N - 1) * sg.K;
+#pragma unroll
+        for (int u = 0; u < GV_U; ++u) {
+            const int k = (b.kc + u) * SC + lane * EPV;
+            wv[u][r] = (u < b.n && k < sg.K) ? ld_stream16(wr + k) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+}
+
+// Step the walker over the next batch of CTA range [.., s_end).
+ES_DEV bool gv_next_batch(GvWalk& w, int& s_next, int s_end, GvBatch& b) {
+    if (s_next >= s_end) return false;
+    const GvLaunch& L = *w.L;
+    const int nck = L.segs[L.ops[w.op].seg0 + w.seg].nck;
+    b.op = w.op; b.tile = w.tile; b.seg = w.seg; b.kc = w.kc;
+    b.n = min(GV_U, min(nck - w.kc, s_end - s_next));
+    b.tile_end = w.advance(b.n);
+    s_next += b.n;
+    b.range_end = s_next == s_end;
+    return true;
+}
+
+// The first batch of CTA `cta`'s range (weights never depend on earlier
+// work, so this may be issued before the inputs are ready).
+template <typename T>
+ES_DEV void gv_prefetch(const GvLaunch& L, int cta, uint4 (&wv)[GV_U][GV_R]) {
+    const int s_begin = cta * L.q;
+    if (s_begin >= L.nstages) return;
+    GvWalk w;
+    w.seek(&L, s_begin);
+    int s_next = s_begin;
+    GvBatch b;
+    gv_next_batch(w, s_next, L.nstages < s_begin + L.q ? L.nstages : s_begin + L.q, b);
+    gv_load_batch<T>(L, b, wv);
+}
+
+// Request stages [s0, s1) of a launch into L2 (no registers held), spread
+// over the calling CTA's threads: one 128-byte line of one row per request.
+// Used by kernels that leave HBM idle to stream in the next weight pass.
+template <typename T>
+ES_DEV void gv_prefetch_l2(const GvLaunch& L, int s0, int s1) {
+    constexpr int LINES = GV_ROW_BYTES / 128;        // lines per row per stage
+    if (s0 >= s1) return;
+    GvWalk w;
+    w.seek(&L, s0);
+    int t = threadIdx.x;
+    for (int s = s0; s < s1; ++s) {
+        const GvOp& o = L.ops[w.op];
+        const GvSeg& sg = L.segs[o.seg0 + w.seg];
+        const size_t rowb = (size_t)sg.K * sizeof(T);
+        const size_t kb = (size_t)w.kc * GV_ROW_BYTES;
+        for (; t < GV_RT * LINES; t += blockDim.x) {
+            const int row = w.tile * GV_RT + t / LINES;
+            const size_t off = kb + (size_t)(t % LINES) * 128;
+            if (row < o.N && off < rowb)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"((const char*)sg.W + (size_t)row * rowb + off));
+        }
+        t -= GV_RT * LINES;
+        w.advance(1);
+    }
+}
+
+// The ops of descriptor L (in shared memory) over CTA `cta`'s stage range,
+// whose first chunk is already in `wpre` (gv_prefetch).  Whole CTA; `xsm` is
+// the dynamic shared memory for the staged activations.
 template <typename T, int M>
-__global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM)
-gv_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __restrict__ counters,
-          int* __restrict__ done) {
+ES_DEV void gv_run(const GvLaunch& L, float* xsm, float* __restrict__ scratch, int* __restrict__ counters,
+                   int cta, const uint4 (&wpre)[GV_U][GV_R]) {
     constexpr int EPV = 16 / sizeof(T);            // weights per 16-byte vector
     constexpr int SC = GV_ROW_BYTES / sizeof(T);   // columns per stage: one vector per lane
     constexpr int NV = GV_R * M;
-    extern __shared__ __align__(16) float xsm[];
-    __shared__ __align__(16) GvLaunch L;
     __shared__ const float* xs_base[GV_MAX_XS];
     __shared__ int xs_stride[GV_MAX_XS];
     __shared__ int s_last;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-    // the launch descriptor: one parallel copy into shared memory
-    {
-        const int4* src = reinterpret_cast<const int4*>(Lg);
-        int4* dst = reinterpret_cast<int4*>(&L);
-        for (int i = tid; i < (int)(sizeof(GvLaunch) / 16); i += GV_THREADS) dst[i] = src[i];
-    }
-    __syncthreads();
     const int Q = L.q;
-    const int s_begin = blockIdx.x * Q;
+    const int s_begin = cta * Q;
     const int s_end = min(L.nstages, s_begin + Q);
+    if (s_begin >= s_end) return;  // (uniform per CTA)
 
     GvWalk w;
     w.seek(&L, s_begin);
     int s_next = s_begin;
-    auto next_batch = [&](GvBatch& b) -> bool {
-        if (s_next >= s_end) return false;
-        b.op = w.op; b.tile = w.tile; b.seg = w.seg; b.kc = w.kc;
-        b.tile_end = w.advance(1);
-        s_next += 1;
-        b.range_end = s_next == s_end;
-        return true;
-    };
-    auto load = [&](const GvBatch& b, uint4 (&wv)[GV_R]) {
-        const GvOp& o = L.ops[b.op];
-        const GvSeg& sg = L.segs[o.seg0 + b.seg];
-        const int k = b.kc * SC + lane * EPV;
-#pragma unroll
-        for (int r = 0; r < GV_R; ++r) {
-            // rows past N read the last row; their sums are dropped
-            const T* wr = (const T*)sg.W + (size_t)min(b.tile * GV_RT + warp * GV_R + r, o.N - 1) * sg.K;
-            wv[r] = k < sg.K ? ld_stream16(wr + k) : make_uint4(0u, 0u, 0u, 0u);
-        }
-    };
-
-    // Weights never depend on the previous kernel: request the first chunk
-    // before griddepcontrol.wait.
     GvBatch cur, nxt;
-    uint4 wc[GV_R], wn[GV_R];
-    bool have = next_batch(cur);
-    if (have) load(cur, wc);
+    uint4 wc[GV_U][GV_R], wn[GV_U][GV_R];
+    bool have = gv_next_batch(w, s_next, s_end, cur);
+#pragma unroll
+    for (int u = 0; u < GV_U; ++u)
+#pragma unroll
+        for (int r = 0; r < GV_R; ++r) wc[u][r] = wpre[u][r];
 
-    grid_dep_wait();
     const int nxs = L.nxs;
     if (tid < nxs) {
         const GvXSrc& x = L.xs[tid];
@@ -297,15 +355,15 @@ gv_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __r
                 const GvXSrc& x = L.xs[i];
                 const int K4 = x.K >> 2, r = t - x.item0, m = r / K4, k = (r - m * K4) * 4;
                 const size_t g = (size_t)(m * x.row_stride + x.row_off) * x.ld + k;
-                v[u] = *reinterpret_cast<const float4*>(x.src + g);
+                v[u] = __ldcg(reinterpret_cast<const float4*>(x.src + g));
                 if (x.add) {
-                    const float4 a = *reinterpret_cast<const float4*>(x.add + g);
+                    const float4 a = __ldcg(reinterpret_cast<const float4*>(x.add + g));
                     v[u].x += a.x; v[u].y += a.y; v[u].z += a.z; v[u].w += a.w;
                 }
                 if (x.kind == XS_NORM) {
                     const T* gp = (const T*)x.gain + k;
                     gn[u] = make_float4(to_f32(gp[0]), to_f32(gp[1]), to_f32(gp[2]), to_f32(gp[3]));
-                    ri[u] = x.rinv[m];
+                    ri[u] = __ldcg(x.rinv + m);
                 }
                 dst[u] = xsm + x.smem_off + (size_t)m * x.K + k;
             }
@@ -324,7 +382,6 @@ gv_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __r
         }
     }
     __syncthreads();
-    grid_dep_launch();
 
     float acc[GV_R][M];
 #pragma unroll
@@ -336,8 +393,8 @@ gv_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __r
     int tile_first = s_begin - ((s_begin - L.ops[cur.op].stage0) % L.ops[cur.op].spt);
 
     while (have) {
-        const bool have_n = next_batch(nxt);
-        if (have_n) load(nxt, wn);  // in flight while this chunk is multiplied
+        const bool have_n = gv_next_batch(w, s_next, s_end, nxt);
+        if (have_n) gv_load_batch<T>(L, nxt, wn);  // in flight while this batch is multiplied
 
         const GvOp& o = L.ops[cur.op];
         const GvSeg& sg = L.segs[o.seg0 + cur.seg];
@@ -352,9 +409,10 @@ gv_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __r
             }
             cur_set = sg.set;
         }
-        {
-            const int k = cur.kc * SC + lane * EPV;
-            if (k < sg.K) gv_fma<T, M>(wc, xs_base[sg.xs] + k, xs_stride[sg.xs], acc);
+#pragma unroll
+        for (int u = 0; u < GV_U; ++u) {
+            const int k = (cur.kc + u) * SC + lane * EPV;
+            if (u < cur.n && k < sg.K) gv_fma<T, M>(wc[u], xs_base[sg.xs] + k, xs_stride[sg.xs], acc);
         }
         if (cur.tile_end || cur.range_end) {
             // ------------ finish the tile (or this CTA's part of it)
@@ -376,7 +434,7 @@ gv_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __r
             bool do_epi = complete;
             if (!complete) {
                 const int sid = s_begin >= tile_first ? 0 : 1;
-                float* part = scratch + ((size_t)(blockIdx.x * 2 + sid) * 2) * GV_THREADS + tid;
+                float* part = scratch + ((size_t)(cta * 2 + sid) * 2) * GV_THREADS + tid;
                 part[0] = v0;
                 if (two) part[GV_THREADS] = v1;
                 __threadfence();
@@ -406,8 +464,8 @@ gv_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __r
                     float* y = o.y + (size_t)m * o.ldy + n;
                     switch (o.epi) {
                         case GEPI_STORE: *y = v0; break;
-                        case GEPI_ACC: *y += v0; break;
-                        case GEPI_ACC_ADD: *y += v0 + o.add[(size_t)m * o.ldy + n]; break;
+                        case GEPI_ACC: *y = __ldcg(y) + v0; break;
+                        case GEPI_ACC_ADD: *y = __ldcg(y) + v0 + __ldcg(o.add + (size_t)m * o.ldy + n); break;
                         default: *y = silu_f(v0) * v1; break;
                     }
                 }
@@ -416,21 +474,39 @@ gv_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __r
         }
         cur = nxt;
 #pragma unroll
-        for (int r = 0; r < GV_R; ++r) wc[r] = wn[r];
+        for (int u = 0; u < GV_U; ++u)
+#pragma unroll
+            for (int r = 0; r < GV_R; ++r) wc[u][r] = wn[u][r];
         have = have_n;
     }
+}
 
-    // ------------ post-norm (1/rms of the next pass's input rows) by the last
-    // CTA to finish
+// One weight-streaming launch as its own kernel.  With programmatic
+// dependent launch the descriptor copy and the first weight chunk overlap
+// the previous kernel's drain.  `done` counts finished CTAs: the last runs
+// the post-norm.
+template <typename T, int M>
+__global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM)
+gv_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __restrict__ counters,
+          int* __restrict__ done) {
+    extern __shared__ __align__(16) float xsm[];
+    __shared__ __align__(16) GvLaunch L;
+    __shared__ int s_done;
+    gv_load_desc(L, Lg);
+    uint4 wpre[GV_U][GV_R];
+    gv_prefetch<T>(L, blockIdx.x, wpre);
+    grid_dep_wait();
+    grid_dep_launch();
+    gv_run<T, M>(L, xsm, scratch, counters, blockIdx.x, wpre);
     if (L.post.rows > 0) {
         __threadfence();
         __syncthreads();
-        if (tid == 0) s_last = atomicAdd(done, 1) == (int)gridDim.x - 1;
+        if (threadIdx.x == 0) s_done = atomicAdd(done, 1) == (int)gridDim.x - 1;
         __syncthreads();
-        if (s_last) {
+        if (s_done) {
             __threadfence();
             post_rinv(L.post);
-            if (tid == 0) *done = 0;
+            if (threadIdx.x == 0) *done = 0;
         }
     }
 }

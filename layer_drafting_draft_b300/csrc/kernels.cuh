@@ -28,57 +28,71 @@ enum { KIND_HOST = 0, KIND_CALIB = 1, KIND_FUZZY = 2, KIND_VERIFY = 3 };
 // KIND_HOST  : row arrays already filled by the host
 // row_base[m] is the first row of m's sequence block (consecutive rows at
 // consecutive positions), which the attention kernel needs.
+struct EmbedArgs {
+    int kind, step, gamma, M;
+    const int* n_commit; const int* tokens; int max_seq; const int* dtok; int gmax;
+    int* row_pos; int* row_seq; int* row_tok; int* row_base;
+    const void* E; float* h; int d, V;
+    int* status;
+    GvPost post;  // 1/rms of the embedded rows (rows map one to one)
+};
+
+// Row m: describe it (sequence, position, token) and gather its embedding.
+// Whole CTA.  Device state written by earlier work is read through L2.
 template <typename T>
-__global__ void prep_embed_kernel(int kind, int step, int gamma, int M,
-                                  const int* __restrict__ n_commit, const int* __restrict__ tokens,
-                                  int max_seq, const int* __restrict__ dtok, int gmax,
-                                  int* row_pos, int* row_seq, int* row_tok, int* row_base,
-                                  const T* __restrict__ E, float* __restrict__ h, int d, int V,
-                                  int* status, GvPost post) {
+ES_DEV void embed_item(const EmbedArgs& a, int m) {
     __shared__ float red[32];
-    grid_dep_wait();
-    const int m = blockIdx.x;
-    if (m >= M) return;
+    __syncthreads();  // shared memory of the previous item
     int b, pos, tok, base = m;
+    const int kind = a.kind, gamma = a.gamma, max_seq = a.max_seq;
     if (kind == KIND_HOST) {
-        b = row_seq[m]; pos = row_pos[m]; tok = row_tok[m]; base = row_base[m];
+        b = __ldcg(a.row_seq + m); pos = __ldcg(a.row_pos + m); tok = __ldcg(a.row_tok + m);
+        base = __ldcg(a.row_base + m);
     } else if (kind == KIND_CALIB) {
         b = m / (gamma + 1);
+        const int nb = __ldcg(a.n_commit + b);
         // first active row of the block (rows before it have no position yet)
-        base = b * (gamma + 1) + max(0, gamma + 1 - n_commit[b]);
+        base = b * (gamma + 1) + max(0, gamma + 1 - nb);
         const int i = m % (gamma + 1);
-        pos = n_commit[b] - (gamma + 1) + i;
+        pos = nb - (gamma + 1) + i;
         if (pos < 0) pos = -1;
-        tok = (pos >= 0 && pos < max_seq) ? tokens[(size_t)b * max_seq + pos] : 0;
+        tok = (pos >= 0 && pos < max_seq) ? __ldcg(a.tokens + (size_t)b * max_seq + pos) : 0;
     } else if (kind == KIND_FUZZY) {
         b = m;
-        pos = n_commit[b] + step - 1;
-        tok = dtok[b * gmax + step - 1];
+        pos = __ldcg(a.n_commit + b) + a.step - 1;
+        tok = __ldcg(a.dtok + b * a.gmax + a.step - 1);
     } else {
         b = m / (gamma + 1);
         base = b * (gamma + 1);
         const int j = m % (gamma + 1);
-        pos = n_commit[b] - 1 + j;
-        tok = j > 0 ? dtok[b * gmax + j - 1] : (pos >= 0 && pos < max_seq) ? tokens[(size_t)b * max_seq + pos] : 0;
+        pos = __ldcg(a.n_commit + b) - 1 + j;
+        tok = j > 0 ? __ldcg(a.dtok + b * a.gmax + j - 1)
+                    : (pos >= 0 && pos < max_seq) ? __ldcg(a.tokens + (size_t)b * max_seq + pos) : 0;
     }
-    if (pos >= max_seq) { if (threadIdx.x == 0) atomicOr(status, STATUS_BAD_POS); pos = -1; }
-    if (tok < 0 || tok >= V) { if (threadIdx.x == 0) atomicOr(status, STATUS_BAD_TOKEN); tok = 0; }
+    if (pos >= max_seq) { if (threadIdx.x == 0) atomicOr(a.status, STATUS_BAD_POS); pos = -1; }
+    if (tok < 0 || tok >= a.V) { if (threadIdx.x == 0) atomicOr(a.status, STATUS_BAD_TOKEN); tok = 0; }
     if (threadIdx.x == 0 && kind != KIND_HOST) {
-        row_pos[m] = pos; row_seq[m] = b; row_tok[m] = tok; row_base[m] = base;
+        a.row_pos[m] = pos; a.row_seq[m] = b; a.row_tok[m] = tok; a.row_base[m] = base;
     }
-    const T* e = E + (size_t)tok * d;
+    const int d = a.d;
+    const T* e = (const T*)a.E + (size_t)tok * d;
     float ss = 0.f;
     for (int i = threadIdx.x; i < d; i += blockDim.x) {
         const float v = to_f32(e[i]);
-        h[(size_t)m * d + i] = v;
+        a.h[(size_t)m * d + i] = v;
         ss += v * v;
     }
-    // 1/rms of the embedded rows for the first weight pass (rows map one to
-    // one here)
-    if (post.rows > 0) {
+    // 1/rms of the embedded rows for the first weight pass
+    if (a.post.rows > 0) {
         ss = block_sum(ss, red);
-        if (threadIdx.x == 0) post.rinv[m] = 1.0f / sqrtf(ss / (float)d + post.eps);
+        if (threadIdx.x == 0) a.post.rinv[m] = 1.0f / sqrtf(ss / (float)d + a.post.eps);
     }
+}
+
+template <typename T>
+__global__ void prep_embed_kernel(EmbedArgs a) {
+    grid_dep_wait();
+    if (blockIdx.x < a.M) embed_item<T>(a, blockIdx.x);
 }
 
 // -------------------------------------------------------------------- RMSNorm

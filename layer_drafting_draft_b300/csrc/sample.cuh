@@ -129,12 +129,12 @@ ES_DEV uint64_t block_locate_chunk(const unsigned long long* mass, int stride, i
 
 ES_DEV bool better(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
 
-__global__ void __launch_bounds__(SM_THREADS) softmax_part_kernel(SampleArgs a) {
+// Item (row r, chunk c) of the partial softmax.  Whole CTA.
+ES_DEV void softmax_part_item(const SampleArgs& a, int r, int c) {
     __shared__ float rv[SM_THREADS / 32];
     __shared__ int ri[SM_THREADS / 32];
-    grid_dep_wait();
-    grid_dep_launch();
-    const int r = blockIdx.x, c = blockIdx.y, b = r / a.per_seq, i = r % a.per_seq + a.off;
+    __syncthreads();  // shared memory of the previous item
+    const int b = r / a.per_seq, i = r % a.per_seq + a.off;
     const float* z = a.z + ((size_t)b * a.ld_rows + i) * a.V;
     const int v0 = c * a.chunk, v1 = min(a.V, v0 + a.chunk);
     const float T = a.greedy > 0 ? 0.f : a.prm->temperature;
@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(SM_THREADS) softmax_part_kernel(SampleArgs a) 
         float bv = -INFINITY;
         int bi = 0x7fffffff;
         for (int v = v0 + tid; v < v1; v += SM_THREADS)
-            if (better(z[v], v, bv, bi)) { bv = z[v]; bi = v; }
+            { const float zv = __ldcg(z + v); if (better(zv, v, bv, bi)) { bv = zv; bi = v; } }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -163,14 +163,14 @@ __global__ void __launch_bounds__(SM_THREADS) softmax_part_kernel(SampleArgs a) 
     }
     const float invT = 1.0f / T;
     float mx = -INFINITY;
-    for (int v = v0 + tid; v < v1; v += SM_THREADS) mx = fmaxf(mx, z[v] * invT);
+    for (int v = v0 + tid; v < v1; v += SM_THREADS) mx = fmaxf(mx, __ldcg(z + v) * invT);
     mx = warp_max(mx);
     if (lane == 0) rv[wid] = mx;
     __syncthreads();
     mx = rv[0];
     for (int w = 1; w < SM_THREADS / 32; ++w) mx = fmaxf(mx, rv[w]);
     float s = 0.f;
-    for (int v = v0 + tid; v < v1; v += SM_THREADS) s += expf(z[v] * invT - mx);
+    for (int v = v0 + tid; v < v1; v += SM_THREADS) s += expf(__ldcg(z + v) * invT - mx);
     s = warp_sum(s);
     __syncthreads();
     if (lane == 0) rv[wid] = s;
@@ -183,14 +183,14 @@ __global__ void __launch_bounds__(SM_THREADS) softmax_part_kernel(SampleArgs a) 
     }
 }
 
-__global__ void __launch_bounds__(SM_THREADS) softmax_finish_kernel(SampleArgs a) {
+// Item (row r, chunk c) of the softmax completion and draw.  Whole CTA.
+ES_DEV void softmax_finish_item(const SampleArgs& a, int r, int c) {
     __shared__ float s_max, s_inv;
     __shared__ unsigned long long rs[SM_THREADS / 32];
     __shared__ uint64_t sh[34];
     __shared__ int s_last;
-    grid_dep_wait();
-    grid_dep_launch();
-    const int r = blockIdx.x, c = blockIdx.y, b = r / a.per_seq, i = r % a.per_seq + a.off;
+    __syncthreads();  // shared memory of the previous item
+    const int b = r / a.per_seq, i = r % a.per_seq + a.off;
     const size_t row = ((size_t)b * a.ld_rows + i) * a.V;
     const float* z = a.z + row;
     float* p = a.p + row;
@@ -200,13 +200,13 @@ __global__ void __launch_bounds__(SM_THREADS) softmax_finish_kernel(SampleArgs a
     const float* part = a.part + (size_t)r * a.nb * 2;
     if (a.greedy > 0 || (a.greedy < 0 && T == 0.f)) {
         // greedy: the logits themselves are kept; the draw is the argmax
-        for (int v = v0 + tid; v < v1; v += SM_THREADS) p[v] = z[v];
+        for (int v = v0 + tid; v < v1; v += SM_THREADS) p[v] = __ldcg(z + v);
         if (a.dtok && c == 0 && tid == 0) {
             float bv = -INFINITY;
             int bi = 0x7fffffff;
             for (int k = 0; k < a.nb; ++k) {
-                const float v = part[2 * k];
-                const int vi = __float_as_int(part[2 * k + 1]);
+                const float v = __ldcg(part + 2 * k);
+                const int vi = __float_as_int(__ldcg(part + 2 * k + 1));
                 if (better(v, vi, bv, bi)) { bv = v; bi = vi; }
             }
             a.dtok[b * a.gmax + i] = bi;
@@ -217,10 +217,10 @@ __global__ void __launch_bounds__(SM_THREADS) softmax_finish_kernel(SampleArgs a
         // the row's max and normaliser: fixed lane assignment and shuffle
         // tree, so every chunk CTA (and every run) gets the same values
         float mx = -INFINITY;
-        for (int k = lane; k < a.nb; k += 32) mx = fmaxf(mx, part[2 * k]);
+        for (int k = lane; k < a.nb; k += 32) mx = fmaxf(mx, __ldcg(part + 2 * k));
         mx = warp_max(mx);
         float s = 0.f;
-        for (int k = lane; k < a.nb; k += 32) s += part[2 * k + 1] * expf(part[2 * k] - mx);
+        for (int k = lane; k < a.nb; k += 32) s += __ldcg(part + 2 * k + 1) * expf(__ldcg(part + 2 * k) - mx);
         s = warp_sum(s);
         if (lane == 0) { s_max = mx; s_inv = 1.0f / s; }
     }
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(SM_THREADS) softmax_finish_kernel(SampleArgs a
     const float invT = 1.0f / T, mx = s_max, inv = s_inv;
     unsigned long long ms = 0;
     for (int v = v0 + tid; v < v1; v += SM_THREADS) {
-        const float pv = expf(z[v] * invT - mx) * inv;
+        const float pv = expf(__ldcg(z + v) * invT - mx) * inv;
         p[v] = pv;
         ms += q40(pv);
     }
@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(SM_THREADS) softmax_finish_kernel(SampleArgs a
     __threadfence();
     // last chunk CTA of the row: locate the draw
     if (tid == 0) a.counters[r] = 0;
-    const uint64_t u = es_draw(a.prm->seed, b, a.phase[b], i, a.gamma);
+    const uint64_t u = es_draw(a.prm->seed, b, __ldcg(a.phase + b), i, a.gamma);
     int ck;
     uint64_t t_rel;
     block_locate_chunk(a.mass + (size_t)r * a.nb, 1, a.nb, u, &ck, &t_rel, sh);
@@ -287,13 +287,14 @@ struct AcceptArgs {
     int* tokens; int max_seq; int* n_commit; const int* n_limit;
 };
 
-__global__ void __launch_bounds__(SM_THREADS) accept_kernel(AcceptArgs a) {
+// Item (sequence b, chunk c) of accept/resample.  Whole CTA.
+ES_DEV void accept_item(const AcceptArgs& a, int b, int c) {
     __shared__ int s_j, s_y, s_last;
     __shared__ int s_am[17];
     __shared__ uint64_t sh[34];
     __shared__ unsigned long long rs[2][SM_THREADS / 32];
-    grid_dep_wait();
-    const int b = blockIdx.x, c = blockIdx.y, g = a.gamma, V = a.V;
+    __syncthreads();  // shared memory of the previous item
+    const int g = a.gamma, V = a.V;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int greedy = a.greedy >= 0 ? a.greedy : (a.prm->temperature == 0.f ? 1 : 0);
     const float* P = a.p + (size_t)b * (g + 1) * V;
@@ -307,8 +308,8 @@ __global__ void __launch_bounds__(SM_THREADS) accept_kernel(AcceptArgs a) {
             float bv = -INFINITY;
             int bi = 0x7fffffff;
             for (int k = lane; k < a.nb; k += 32) {
-                const float v = gp[2 * k];
-                const int vi = __float_as_int(gp[2 * k + 1]);
+                const float v = __ldcg(gp + 2 * k);
+                const int vi = __float_as_int(__ldcg(gp + 2 * k + 1));
                 if (better(v, vi, bv, bi)) { bv = v; bi = vi; }
             }
 #pragma unroll
@@ -323,24 +324,24 @@ __global__ void __launch_bounds__(SM_THREADS) accept_kernel(AcceptArgs a) {
         if (tid == 0) {
             int j = g;
             for (int i = 0; i < g; ++i)
-                if (s_am[i] != d[i]) { j = i; break; }
+                if (s_am[i] != __ldcg(d + i)) { j = i; break; }
             s_j = j;
             s_y = s_am[j];
         }
     } else {
         uint64_t seed = 0;
         int64_t ph = 0;
-        if (!a.u_explicit) { seed = a.prm->seed; ph = a.phase[b]; }
+        if (!a.u_explicit) { seed = a.prm->seed; ph = __ldcg(a.phase + b); }
         auto draw = [&](int t) -> uint64_t {  // t = 0..g (accept tests, then the residual)
             return a.u_explicit ? a.u_explicit[(size_t)b * (g + 1) + t] : es_draw(seed, b, ph, g + t, g);
         };
         if (tid == 0) {
             int j = g;
             for (int i = 0; i < g; ++i) {
-                const int x = d[i];
+                const int x = __ldcg(d + i);
                 if (x < 0 || x >= V) { j = i; break; }  // not a token: rejected
                 const float u = uniform24(draw(i));
-                if (!(__fmul_rn(u, Q[(size_t)i * V + x]) < P[(size_t)i * V + x])) { j = i; break; }
+                if (!(__fmul_rn(u, __ldcg(Q + (size_t)i * V + x)) < __ldcg(P + (size_t)i * V + x))) { j = i; break; }
             }
             s_j = j;
         }
@@ -351,9 +352,9 @@ __global__ void __launch_bounds__(SM_THREADS) accept_kernel(AcceptArgs a) {
         const int v0 = c * a.chunk, v1 = min(V, v0 + a.chunk);
         unsigned long long mr = 0, mp = 0;
         for (int v = v0 + tid; v < v1; v += SM_THREADS) {
-            const float pv = Pj[v];
+            const float pv = __ldcg(Pj + v);
             mp += q40(pv);
-            mr += j < g ? q40(fmaxf(0.f, __fsub_rn(pv, Qj[v]))) : q40(pv);
+            mr += j < g ? q40(fmaxf(0.f, __fsub_rn(pv, __ldcg(Qj + v)))) : q40(pv);
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -390,8 +391,8 @@ __global__ void __launch_bounds__(SM_THREADS) accept_kernel(AcceptArgs a) {
             const bool resid = j < g && !use_p;
             y = c0 + block_find_q40(
                          [&](int k) {
-                             const float pv = Pj[c0 + k];
-                             return resid ? fmaxf(0.f, __fsub_rn(pv, Qj[c0 + k])) : pv;
+                             const float pv = __ldcg(Pj + c0 + k);
+                             return resid ? fmaxf(0.f, __fsub_rn(pv, __ldcg(Qj + c0 + k))) : pv;
                          },
                          c1 - c0, t_rel, sh);
         }
@@ -402,16 +403,31 @@ __global__ void __launch_bounds__(SM_THREADS) accept_kernel(AcceptArgs a) {
         const int j = s_j, y = s_y;
         a.n_acc[b] = j;
         int* ot = a.out_tok + (size_t)b * (g + 1);
-        for (int t = 0; t <= g; ++t) ot[t] = t < j ? d[t] : (t == j ? y : -1);
-        if (a.tokens && a.n_commit[b] < a.n_limit[b]) {
-            const int n = a.n_commit[b];
+        for (int t = 0; t <= g; ++t) ot[t] = t < j ? __ldcg(d + t) : (t == j ? y : -1);
+        if (a.tokens && __ldcg(a.n_commit + b) < __ldcg(a.n_limit + b)) {
+            const int n = __ldcg(a.n_commit + b);
             int* tk = a.tokens + (size_t)b * a.max_seq;
-            for (int t = 0; t < j && n + t < a.max_seq; ++t) tk[n + t] = d[t];
+            for (int t = 0; t < j && n + t < a.max_seq; ++t) tk[n + t] = __ldcg(d + t);
             if (n + j < a.max_seq) tk[n + j] = y;
             a.n_commit[b] = n + j + 1;
-            a.phase[b] += 1;
+            a.phase[b] = __ldcg(a.phase + b) + 1;
         }
     }
+}
+
+__global__ void __launch_bounds__(SM_THREADS) softmax_part_kernel(SampleArgs a) {
+    grid_dep_wait();
+    grid_dep_launch();
+    softmax_part_item(a, blockIdx.x, blockIdx.y);
+}
+__global__ void __launch_bounds__(SM_THREADS) softmax_finish_kernel(SampleArgs a) {
+    grid_dep_wait();
+    grid_dep_launch();
+    softmax_finish_item(a, blockIdx.x, blockIdx.y);
+}
+__global__ void __launch_bounds__(SM_THREADS) accept_kernel(AcceptArgs a) {
+    grid_dep_wait();
+    accept_item(a, blockIdx.x, blockIdx.y);
 }
 
 }  // namespace es

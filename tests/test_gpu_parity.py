@@ -168,3 +168,4 @@ def test_bf16_logits_within_tolerance(mode, k):
     assert st["maxabs_q"] <= BF16_MAXABS and st["maxabs_p"] <= BF16_MAXABS
     assert st["rell2"] <= BF16_RELL2
     g.close()
+
