@@ -197,6 +197,29 @@ ES_API es_status es_accept_resample(const float *p, const float *q, const int32_
                              int greedy, int32_t *n_acc, int32_t *tok,
                              void *stream);
 
+/* es_accept_resample without any device allocation.  The pages have no
+ * counterpart: this is for callers that cannot allocate device memory at the
+ * point of the call -- code running while a CUDA stream is being captured
+ * into a graph (cudaMalloc is not allowed there), latency-critical loops that
+ * cannot take cudaMalloc's device-wide synchronisation, and hosts whose
+ * device memory is owned by their own allocator.  es_accept_resample
+ * allocates its scratch (per-chunk partials, masses, arrival counters) on
+ * every call; this entry point uses a fixed array inside the library instead.
+ *   Limits: B <= 16, gamma <= 16, and at most 160 vocabulary chunks (a chunk
+ *   is max(512, ceil(V / SMs)) entries; 148 on a B300 for any V).  Larger
+ *   sizes return ES_ERR_ARG (with a message on stderr).
+ *   The array is shared by every call in the process on a device and keeps
+ *   the last call's contents (the counters are cleared at each call): calls
+ *   that overlap on the GPU -- on different streams, or from several host
+ *   threads -- race and must not be issued.
+ *   The first call on a device looks up the array's device address; make it
+ *   before any stream capture that should contain later calls.
+ * Arguments, layouts and results as es_accept_resample; synchronous on
+ * `stream`. */
+ES_API es_status es_accept_resample_noalloc(const float *p, const float *q, const int32_t *d,
+                                            const uint64_t *u, int B, int gamma, int V, int greedy,
+                                            int32_t *n_acc, int32_t *tok, void *stream);
+
 /* Integer-quantised categorical draw alone ([SD] sampling step, quantised
  * as the oracle does): for each of B rows of unnormalised float32 weights
  * w [B, V] (device) and one draw u [B] (device), writes the index to

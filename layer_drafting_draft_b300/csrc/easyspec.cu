@@ -11,6 +11,7 @@
 #include <cstring>
 #include <map>
 #include <memory>
+#include <mutex>
 #include <string>
 #include <tuple>
 #include <vector>
@@ -991,6 +992,43 @@ es_stats do_decode(es_ctx* c, int max_new, int gamma, int k, float temperature, 
 
 }  // namespace
 
+// ------------------------------------------------------------------ fixed scratch
+// Scratch of es_accept_resample_noalloc: a file-scope device array, so the
+// entry point never allocates.  Every GPU that loads the library holds it
+// until the process exits.  Layout: greedy argmax partials
+// [NOALLOC_MAX_B * 17 rows][NOALLOC_MAX_NB][2] floats, chunk masses
+// [NOALLOC_MAX_B][NOALLOC_MAX_NB][2] u64, arrival counters [NOALLOC_MAX_B].
+constexpr int NOALLOC_MAX_B = 16;
+constexpr int NOALLOC_MAX_GAMMA = 16;
+constexpr int NOALLOC_MAX_NB = 160;
+constexpr size_t NA_GPART_BYTES = (size_t)NOALLOC_MAX_B * (NOALLOC_MAX_GAMMA + 1) * NOALLOC_MAX_NB * 2 * sizeof(float);
+constexpr size_t NA_MASS_BYTES = (size_t)NOALLOC_MAX_B * NOALLOC_MAX_NB * 2 * sizeof(unsigned long long);
+constexpr size_t NA_CTR_BYTES = (size_t)NOALLOC_MAX_B * sizeof(int);
+constexpr size_t NA_BYTES = NA_GPART_BYTES + NA_MASS_BYTES + NA_CTR_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NA_BYTES];
+
+// Device address of the scratch array on the current device.  Host code
+// cannot use the array's name as a device pointer; the address is looked up
+// once per device (the first call on that device) and kept.
+es_status noalloc_scratch(unsigned char** out) {
+    constexpr int MAX_DEV = 64;
+    static unsigned char* addr[MAX_DEV] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEV) return ES_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+            cudaGetLastError();
+            return ES_ERR_CUDA;
+        }
+        addr[dev] = static_cast<unsigned char*>(p);
+    }
+    *out = addr[dev];
+    return ES_OK;
+}
+
 // =================================================================== C ABI
 extern "C" {
 
@@ -1250,6 +1288,49 @@ es_status es_accept_resample(const float* p, const float* q, const int32_t* d, c
     cudaFree(mass);
     cudaFree(ctr);
     return rc;
+}
+
+es_status es_accept_resample_noalloc(const float* p, const float* q, const int32_t* d, const uint64_t* u,
+                                     int B, int gamma, int V, int greedy, int32_t* n_acc, int32_t* tok,
+                                     void* stream) {
+    if (!p || !q || !d || !n_acc || !tok || B < 1 || gamma < 1 || V < 1) return ES_ERR_ARG;
+    if (!greedy && !u) return ES_ERR_ARG;
+    int dev = 0, nsm = 148;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return ES_ERR_CUDA;
+    AcceptArgs a;
+    memset(&a, 0, sizeof a);
+    vocab_chunks(V, nsm, &a.chunk, &a.nb);
+    if (B > NOALLOC_MAX_B || gamma > NOALLOC_MAX_GAMMA || a.nb > NOALLOC_MAX_NB) {
+        fprintf(stderr, "es_accept_resample_noalloc: B=%d gamma=%d (%d vocabulary chunks) beyond the fixed "
+                        "scratch (B <= %d, gamma <= %d, chunks <= %d)\n",
+                B, gamma, a.nb, NOALLOC_MAX_B, NOALLOC_MAX_GAMMA, NOALLOC_MAX_NB);
+        return ES_ERR_ARG;
+    }
+    unsigned char* base = nullptr;
+    const es_status sst = noalloc_scratch(&base);
+    if (sst != ES_OK) return sst;
+    cudaStream_t st = (cudaStream_t)stream;
+    a.p = p; a.q = q; a.d = d; a.gmax = gamma; a.gamma = gamma; a.V = V; a.greedy = greedy ? 1 : 0;
+    a.u_explicit = u; a.n_acc = n_acc; a.out_tok = tok;
+    float* gpart = reinterpret_cast<float*>(base);
+    a.gpart = gpart;
+    a.mass = reinterpret_cast<unsigned long long*>(base + NA_GPART_BYTES);
+    a.counters = reinterpret_cast<int*>(base + NA_GPART_BYTES + NA_MASS_BYTES);
+    // the arrival counters must start at zero (the array keeps the last
+    // call's contents)
+    if (cudaMemsetAsync(a.counters, 0, (size_t)B * sizeof(int), st) != cudaSuccess) return ES_ERR_CUDA;
+    if (greedy) {
+        SampleArgs s;
+        memset(&s, 0, sizeof s);
+        s.z = p; s.V = V; s.chunk = a.chunk; s.nb = a.nb; s.per_seq = 1; s.off = 0; s.ld_rows = 1;
+        s.greedy = 1; s.part = gpart;
+        softmax_part_kernel<<<dim3((unsigned)(B * (gamma + 1)), a.nb), SM_THREADS, 0, st>>>(s);
+    }
+    accept_kernel<<<dim3(B, a.nb), SM_THREADS, 0, st>>>(a);
+    if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess) return ES_ERR_CUDA;
+    return ES_OK;
 }
 
 es_status es_sample(const float* w, const uint64_t* u, int B, int V, int32_t* idx, void* stream) {

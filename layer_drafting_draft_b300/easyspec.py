@@ -25,6 +25,7 @@ STATUS_NAMES = {0: "ES_OK", -1: "ES_ERR_ARG", -2: "ES_ERR_OOM", -3: "ES_ERR_CUDA
 
 EXPORTED = ["easyspec_init", "easyspec_prefill", "calibrate_kv", "draft_step", "verify_step",
             "generate", "es_decode", "es_profile", "es_profile_read", "es_accept_resample",
+            "es_accept_resample_noalloc",
             "es_sample", "es_read_kv", "es_read_dist", "es_read_tokens", "easyspec_last_error",
             "easyspec_destroy"]
 
@@ -82,6 +83,7 @@ def lib() -> C.CDLL:
             "es_profile": ([ctxp, C.c_int], C.c_int),
             "es_profile_read": ([ctxp, C.c_int, C.c_char_p, C.c_int, C.POINTER(C.c_double), C.POINTER(C.c_int64), C.POINTER(C.c_double)], C.c_int),
             "es_accept_resample": ([vp, vp, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, vp, vp, vp], C.c_int),
+            "es_accept_resample_noalloc": ([vp, vp, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, vp, vp, vp], C.c_int),
             "es_sample": ([vp, vp, C.c_int, C.c_int, vp, vp], C.c_int),
             "es_read_kv": ([ctxp, C.c_int, C.c_int, C.c_int, C.c_int, f32p, f32p], C.c_int),
             "es_read_dist": ([ctxp, C.c_int, f32p], C.c_int),
@@ -262,6 +264,22 @@ def es_accept_resample(p: torch.Tensor, q: torch.Tensor, d: torch.Tensor, u: tor
                                   torch.cuda.current_stream().cuda_stream)
     if st != ES_OK:
         raise EasySpecError(st, "es_accept_resample")
+    return n_acc, tok
+
+
+def es_accept_resample_noalloc(p: torch.Tensor, q: torch.Tensor, d: torch.Tensor, u: torch.Tensor | None,
+                               greedy: bool):
+    """es_accept_resample through the entry point that allocates no device
+    memory (fixed scratch inside the library; B <= 16, gamma <= 16).
+    Only the outputs are allocated here, by the caller's side."""
+    B, g1, V = p.shape
+    n_acc = torch.empty(B, dtype=torch.int32, device=p.device)
+    tok = torch.empty(B, g1, dtype=torch.int32, device=p.device)
+    st = lib().es_accept_resample_noalloc(_ptr(p), _ptr(q), _ptr(d), _ptr(u) if u is not None else None,
+                                          B, g1 - 1, V, 1 if greedy else 0, _ptr(n_acc), _ptr(tok),
+                                          torch.cuda.current_stream().cuda_stream)
+    if st != ES_OK:
+        raise EasySpecError(st, "es_accept_resample_noalloc")
     return n_acc, tok
 
 
