@@ -18,7 +18,6 @@
 // merges them in split order and writes the head outputs.
 #pragma once
 #include "common.cuh"
-#include "gemv.cuh"
 
 namespace es {
 
@@ -48,8 +47,6 @@ struct AttnArgs {
     float* part;   // [M][nl][H][nsplit][hd + 2]
     int* counters; // [M][nl][Hkv]
     const int* row_pos; const int* row_seq; const int* row_base;
-    const GvLaunch* next;  // the weight pass that follows (its weights are requested into L2), or null
-    int next_bf16;
 };
 
 // dynamic shared memory (floats): qs G*(hd+4) | ks 64*(hd+4) | vs 64*(hd+4) |
@@ -265,16 +262,6 @@ template <typename T>
 __global__ void __launch_bounds__(ATT_THREADS) attn_kernel(AttnArgs a) {
     grid_dep_wait();
     grid_dep_launch();
-    // Attention leaves HBM mostly idle: stream this CTA's share of the next
-    // weight pass into L2 first (its weights do not depend on anything).
-    if (a.next) {
-        const int cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
-        const int ncta = gridDim.x * gridDim.y * gridDim.z;
-        const int ns = a.next->nstages;
-        const int s0 = (int)((long)ns * cta / ncta), s1 = (int)((long)ns * (cta + 1) / ncta);
-        if (a.next_bf16) gv_prefetch_l2<bf16>(*a.next, s0, s1);
-        else gv_prefetch_l2<float>(*a.next, s0, s1);
-    }
     attn_item<T>(a, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 

@@ -51,7 +51,6 @@ struct Rec {
     double bytes = 0;          // algorithmic bytes (weights + activations), 0 if not modelled
     const GvLaunch* gv = nullptr;           // device copy (after upload)
     std::shared_ptr<GvLaunch> host;         // host copy while the plan is built
-    size_t next_gv = 0;                     // attention: index of the weight pass after it
     bool bf16 = false;                      // weights are bf16
     int grid = 0, smem = 0, M = 0, ntiles64 = 0;
     NormArgs norm{};
@@ -396,9 +395,6 @@ Rec finish_gv(es_ctx* c, GvBuild& b, const char* name) {
 }
 
 void upload_plan(es_ctx* c, Plan& p) {
-    // each attention launch streams in the weights of the pass after it
-    for (size_t i = 0; i + 1 < p.recs.size(); ++i)
-        if (p.recs[i].kind == R_ATTN && p.recs[i + 1].kind == R_GV) p.recs[i].next_gv = i + 1;
     for (Rec& r : p.recs) {
         if (!r.host) continue;
         const size_t bytes = sizeof(GvLaunch);
@@ -409,11 +405,6 @@ void upload_plan(es_ctx* c, Plan& p) {
         r.gv = reinterpret_cast<const GvLaunch*>(c->arena + at);
         r.host.reset();
     }
-    for (Rec& r : p.recs)
-        if (r.next_gv) {
-            r.attn.next = p.recs[r.next_gv].gv;
-            r.attn.next_bf16 = r.bf16 ? 1 : 0;
-        }
 }
 
 NormArgs norm_args(Model& m, float* h, const float* add) {

@@ -269,32 +269,6 @@ ES_DEV void gv_prefetch(const GvLaunch& L, int cta, uint4 (&wv)[GV_U][GV_R]) {
     gv_load_batch<T>(L, b, wv);
 }
 
-// Request stages [s0, s1) of a launch into L2 (no registers held), spread
-// over the calling CTA's threads: one 128-byte line of one row per request.
-// Used by kernels that leave HBM idle to stream in the next weight pass.
-template <typename T>
-ES_DEV void gv_prefetch_l2(const GvLaunch& L, int s0, int s1) {
-    constexpr int LINES = GV_ROW_BYTES / 128;        // lines per row per stage
-    if (s0 >= s1) return;
-    GvWalk w;
-    w.seek(&L, s0);
-    int t = threadIdx.x;
-    for (int s = s0; s < s1; ++s) {
-        const GvOp& o = L.ops[w.op];
-        const GvSeg& sg = L.segs[o.seg0 + w.seg];
-        const size_t rowb = (size_t)sg.K * sizeof(T);
-        const size_t kb = (size_t)w.kc * GV_ROW_BYTES;
-        for (; t < GV_RT * LINES; t += blockDim.x) {
-            const int row = w.tile * GV_RT + t / LINES;
-            const size_t off = kb + (size_t)(t % LINES) * 128;
-            if (row < o.N && off < rowb)
-                asm volatile("prefetch.global.L2 [%0];" ::"l"((const char*)sg.W + (size_t)row * rowb + off));
-        }
-        t -= GV_RT * LINES;
-        w.advance(1);
-    }
-}
-
 // The ops of descriptor L (in shared memory) over CTA `cta`'s stage range,
 // whose first chunk is already in `wpre` (gv_prefetch).  Whole CTA; `xsm` is
 // the dynamic shared memory for the staged activations.

@@ -5,7 +5,9 @@
 
 After the prompt prefill and `--warmup-phases` untimed phases, `--phases`
 phases (draft_step + verify_step) run inside the NVTX range "measure", so an
-`ncu --nvtx --nvtx-include measure/` capture sees exactly their launches.
+`ncu --nvtx --nvtx-include measure/` capture sees exactly their launches;
+each draft_step / verify_step sits in a nested range "draft" / "verify"
+(`--nvtx-include measure/verify/` selects the base model's launches).
 With --table the same phases run a second time with per-launch CUDA-event
 timing and a per-kernel table (time, launches, algorithmic bytes, GB/s) is
 printed.  --base-layers / --draft-layers truncate the models (same widths)
@@ -57,8 +59,12 @@ def main(argv=None):
 
     def phases(n, s0):
         for i in range(n):
+            torch.cuda.nvtx.range_push("draft")
             g.draft_step(k, gamma, a.temperature, s0 + i)
+            torch.cuda.nvtx.range_pop()
+            torch.cuda.nvtx.range_push("verify")
             g.verify_step(a.temperature, s0 + i, gamma)
+            torch.cuda.nvtx.range_pop()
 
     g.easyspec_prefill(prompt)
     phases(a.warmup_phases, 100)
