@@ -12,7 +12,9 @@
 #include <map>
 #include <memory>
 #include <mutex>
+#include <set>
 #include <string>
+#include <type_traits>
 #include <tuple>
 #include <vector>
 
@@ -72,6 +74,7 @@ struct Model {
     int L = 0, d = 0, H = 0, Hkv = 0, hd = 0, F = 0, V = 0, qd = 0, kvd = 0, dtype = 0;
     float theta = 0, eps = 0;
     size_t esz = 4;
+    const char* tag = "";  // "draft" / "base": prefix of the profiling labels
     const void *embed = nullptr, *lm = nullptr, *fnorm = nullptr;
     std::vector<Layer> ly;
     KVGeom g{};
@@ -234,6 +237,7 @@ void setup_model(es_ctx* c, Model& m, const es_model_shape& s, const es_weights*
                  int slots, const char* which) {
     check_shape(s, which);
     if (!w) arg_fail(ES_ERR_ARG, "%s: null weights", which);
+    m.tag = which;
     m.L = s.n_layers; m.d = s.d; m.H = s.n_heads; m.Hkv = s.n_kv_heads; m.hd = s.head_dim;
     m.F = s.ffn; m.V = s.vocab; m.qd = m.H * m.hd; m.kvd = m.Hkv * m.hd; m.dtype = s.dtype;
     m.theta = s.rope_theta; m.eps = s.eps; m.esz = s.dtype == ES_DTYPE_BF16 ? 2 : 4;
@@ -297,6 +301,14 @@ void setup_model(es_ctx* c, Model& m, const es_model_shape& s, const es_weights*
     m.row_base = c->dalloc<int>(Mw);
 }
 
+// Profiling label "<model>.<step>", interned so records can keep a pointer.
+const char* label(const Model& m, const char* step) {
+    static std::mutex mu;
+    static std::set<std::string> names;
+    std::lock_guard<std::mutex> lock(mu);
+    return names.insert(std::string(m.tag) + "." + step).first->c_str();
+}
+
 // ------------------------------------------------------------------ GEMV launch building
 // Collects the ops and activation sources of one weight-streaming launch.
 struct GvBuild {
@@ -304,17 +316,22 @@ struct GvBuild {
     size_t esz;
     int xfloats = 0;
     bool simt;  // many-row launch (SIMT GEMM): every source read from global memory
-    GvBuild(int M, size_t esz_, bool simt_) : L(std::make_shared<GvLaunch>()), esz(esz_), simt(simt_) {
+    bool mma;   // bf16 weights, few rows: tensor-core kernel (16-row tiles, hi/lo planes)
+    GvBuild(int M, size_t esz_, bool simt_)
+        : L(std::make_shared<GvLaunch>()), esz(esz_), simt(simt_), mma(esz_ == 2 && !simt_) {
         memset(L.get(), 0, sizeof(GvLaunch));
         L->M = M;
     }
     // An activation source: rows r*rs + ro of src (leading dimension ld).
-    // Staged in shared memory while room is left, else read from global.
+    // SIMT-FMA kernel: staged in shared memory while room is left, else read
+    // from global.  Tensor-core kernel: each CTA stages the windows it needs
+    // while its budget lasts (decided on the device).
     int source(const float* src, int K, int ld, int rs = 1, int ro = 0) {
         if (L->nxs >= GV_MAX_XS) arg_fail(ES_ERR_ARG, "too many activation sources in one launch");
         const int need = L->M * K;
         int off = -1;
-        if (!simt && xfloats + need <= GV_XSMEM_MAX) { off = xfloats; xfloats += (need + 3) & ~3; }
+        if (mma) off = 0;
+        else if (!simt && xfloats + need <= GV_XSMEM_MAX) { off = xfloats; xfloats += (need + 3) & ~3; }
         GvXSrc& x = L->xs[L->nxs];
         x.src = src; x.K = K; x.ld = ld; x.row_stride = rs; x.row_off = ro; x.smem_off = off; x.kind = XS_RAW;
         return L->nxs++;
@@ -322,7 +339,7 @@ struct GvBuild {
     // A normalised source (h + add) * rinv * gain, rows r*rs + ro of h; -1
     // when it does not fit in shared memory (the caller normalises it first).
     int norm_source(const float* h, const float* add, const void* gain, const float* rinv, int K, int rs, int ro) {
-        if (simt || xfloats + L->M * K > GV_XSMEM_MAX) return -1;
+        if (simt || (!mma && xfloats + L->M * K > GV_XSMEM_MAX)) return -1;
         const int i = source(h, K, K, rs, ro);
         GvXSrc& x = L->xs[i];
         x.kind = XS_NORM; x.add = add; x.gain = gain; x.rinv = rinv;
@@ -344,6 +361,7 @@ struct GvBuild {
         if (o.seg0 + o.nseg != nsegs) arg_fail(ES_ERR_ARG, "internal: segments out of order");
         if (o.nseg >= GV_MAX_SEG || nsegs >= GV_MAX_SEGS) arg_fail(ES_ERR_ARG, "too many K-concatenated segments");
         if (xs < 0 || L->xs[xs].K != K) arg_fail(ES_ERR_ARG, "segment / source width mismatch");
+        if (mma && K % 8) arg_fail(ES_ERR_ARG, "bf16 weight rows must be a multiple of 8 elements (K = %d)", K);
         GvSeg& s = L->segs[nsegs];
         s.W = W; s.K = K; s.xs = xs; s.set = set;
         o.nseg++;
@@ -353,7 +371,10 @@ struct GvBuild {
 // Stage bookkeeping; the descriptor stays on the host until upload_plan().
 Rec finish_gv(es_ctx* c, GvBuild& b, const char* name) {
     GvLaunch& L = *b.L;
-    const int SC = GV_ROW_BYTES / (int)b.esz;
+    // chunk columns and tile rows: 512-byte x 32-row stages (SIMT-FMA kernel)
+    // or 128-column x 128-row stages (tensor-core kernel)
+    const int SC = b.mma ? GVM_COLS : GV_ROW_BYTES / (int)b.esz;
+    const int RT = b.mma ? GVM_BLOCK : GV_RT;
     int t = 0, st = 0, t64 = 0;
     double wbytes = 0, rowbytes = 0;
     for (int i = 0; i < L.nops; ++i) {
@@ -365,7 +386,7 @@ Rec finish_gv(es_ctx* c, GvBuild& b, const char* name) {
             o.spt += sg.nck;
             wbytes += (double)o.N * sg.K * b.esz;
         }
-        o.ntiles = (o.N + GV_RT - 1) / GV_RT;
+        o.ntiles = (o.N + RT - 1) / RT;
         o.tile0 = t; o.stage0 = st; o.tile64_0 = t64;
         t += o.ntiles; st += o.ntiles * o.spt; t64 += (o.N + GB - 1) / GB;
         rowbytes += (double)o.N * 4.0 * (o.epi == GEPI_STORE || o.epi == GEPI_SWIGLU ? 1 : o.epi == GEPI_ACC ? 2 : 3);
@@ -374,11 +395,11 @@ Rec finish_gv(es_ctx* c, GvBuild& b, const char* name) {
     L.ntiles = t; L.nstages = st; L.ntiles64 = t64;
     const int ctas = c->num_sms * GV_CTAS_PER_SM;
     L.q = std::max(1, (st + ctas - 1) / ctas);
-    L.x_smem_floats = b.xfloats;
+    L.x_smem_floats = b.mma ? GV_XSMEM_MAX : b.xfloats;
     int items = 0;  // staging items (4 columns of one row) of the shared-memory sources
     for (int i = 0; i < L.nxs; ++i) {
         L.xs[i].item0 = items;
-        if (L.xs[i].smem_off >= 0) items += L.M * (L.xs[i].K / 4);
+        if (!b.mma && L.xs[i].smem_off >= 0) items += L.M * (L.xs[i].K / 4);
     }
     L.x_items = items;
     if (t > GV_COUNTERS) arg_fail(ES_ERR_ARG, "launch has %d tiles (> %d)", t, GV_COUNTERS);
@@ -387,7 +408,19 @@ Rec finish_gv(es_ctx* c, GvBuild& b, const char* name) {
     r.name = name;
     r.M = L.M;
     r.grid = (st + L.q - 1) / L.q;
-    r.smem = b.xfloats * (int)sizeof(float);
+    if (b.mma) {
+        // shared memory: the largest staged window set of any CTA (the device
+        // repeats this computation with the result as its budget)
+        int need = 0;
+        for (int cta = 0; cta < r.grid; ++cta) {
+            GvmWin win[GVM_NWIN];
+            int items, used;
+            gvm_windows(L, cta * L.q, std::min(st, (cta + 1) * L.q), win, GV_XSMEM_MAX, &items, &used);
+            need = std::max(need, used);
+        }
+        L.x_smem_floats = need;
+    }
+    r.smem = L.x_smem_floats * (int)sizeof(float);
     r.ntiles64 = t64;
     r.bytes = wbytes + L.M * rowbytes;
     r.host = b.L;
@@ -486,7 +519,7 @@ Plan build_forward(es_ctx* c, Model& m, const std::vector<std::vector<int>>& gro
         return b.source(buf, m.d, m.d);
     };
     auto push_gv = [&](GvBuild& b, const char* name) {
-        P.recs.push_back(finish_gv(c, b, name));
+        P.recs.push_back(finish_gv(c, b, label(m, name)));
         writer = (int)P.recs.size() - 1;
     };
     auto raw = [&](GvBuild& b, const float* p, int K) { return b.source(p, K, K); };
@@ -520,6 +553,7 @@ Plan build_forward(es_ctx* c, Model& m, const std::vector<std::vector<int>>& gro
             push_gv(b, full ? "gv_qkv_gateup" : "gv_qkv");
         }
         P.recs.push_back(attn_rec(c, m, l0, n, M));
+        P.recs.back().name = label(m, "attention");
         if (full) {
             // K-concatenated [Wo_1 .. Wo_n, Wdown_1 .. Wdown_n] . [a_1..a_n, s_1..s_n]
             GvBuild b(M, m.esz, !fast);
@@ -603,16 +637,21 @@ template <typename T>
 void run_rec(es_ctx* c, const Rec& r) {
     switch (r.kind) {
         case R_GV:
-            switch (r.M) {
+            if constexpr (std::is_same<T, bf16>::value) {
+                launch(c, r.name, r.bytes, gvm_kernel, dim3(r.grid), dim3(GV_THREADS), (size_t)r.smem, r.gv,
+                       c->gv_scratch, c->gv_counters, c->gv_done);
+            } else {
+                switch (r.M) {
 #define ES_GV_CASE(MM)                                                                              \
     case MM:                                                                                        \
         launch(c, r.name, r.bytes, gv_kernel<T, MM>, dim3(r.grid), dim3(GV_THREADS), (size_t)r.smem, \
                r.gv, c->gv_scratch, c->gv_counters, c->gv_done);                                    \
         break;
-                ES_GV_CASE(1) ES_GV_CASE(2) ES_GV_CASE(3) ES_GV_CASE(4)
-                ES_GV_CASE(5) ES_GV_CASE(6) ES_GV_CASE(7) ES_GV_CASE(8)
+                    ES_GV_CASE(1) ES_GV_CASE(2) ES_GV_CASE(3) ES_GV_CASE(4)
+                    ES_GV_CASE(5) ES_GV_CASE(6) ES_GV_CASE(7) ES_GV_CASE(8)
 #undef ES_GV_CASE
-                default: arg_fail(ES_ERR_ARG, "internal: GEMV rows %d", r.M);
+                    default: arg_fail(ES_ERR_ARG, "internal: GEMV rows %d", r.M);
+                }
             }
             break;
         case R_GEMM:
@@ -1083,7 +1122,7 @@ es_status easyspec_init(const es_config* cfg, const es_weights* draft, const es_
         c->status = c->dalloc<int>(1);
         c->arena_cap = (size_t)64 << 20;
         c->arena = c->dalloc<char>(c->arena_cap);
-        c->gv_scratch = c->dalloc<float>(GV_SCRATCH_FLOATS);
+        c->gv_scratch = c->dalloc<float>(std::max(GV_SCRATCH_FLOATS, GVM_SCRATCH_FLOATS));
         c->gv_counters = c->dalloc<int>(GV_COUNTERS);
         c->gv_done = c->dalloc<int>(1);
         c->att_counters = c->dalloc<int>(ATT_COUNTERS);
@@ -1096,11 +1135,10 @@ es_status easyspec_init(const es_config* cfg, const es_weights* draft, const es_
         const int gv_smem = GV_XSMEM_MAX * (int)sizeof(float);
 #define ES_GV_ATTR(TT, MM) \
         CK(cudaFuncSetAttribute(gv_kernel<TT, MM>, cudaFuncAttributeMaxDynamicSharedMemorySize, gv_smem));
-        ES_GV_ATTR(bf16, 1) ES_GV_ATTR(bf16, 2) ES_GV_ATTR(bf16, 3) ES_GV_ATTR(bf16, 4)
-        ES_GV_ATTR(bf16, 5) ES_GV_ATTR(bf16, 6) ES_GV_ATTR(bf16, 7) ES_GV_ATTR(bf16, 8)
         ES_GV_ATTR(float, 1) ES_GV_ATTR(float, 2) ES_GV_ATTR(float, 3) ES_GV_ATTR(float, 4)
         ES_GV_ATTR(float, 5) ES_GV_ATTR(float, 6) ES_GV_ATTR(float, 7) ES_GV_ATTR(float, 8)
 #undef ES_GV_ATTR
+        CK(cudaFuncSetAttribute(gvm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, gv_smem));
         const int att_smem = 200 * 1024;
         CK(cudaFuncSetAttribute(attn_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, att_smem));
         CK(cudaFuncSetAttribute(attn_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, att_smem));

@@ -107,7 +107,7 @@ ES_DEV float silu_f(float g) { return g / (1.0f + expf(-g)); }
 struct GvWalk {
     const GvLaunch* L;
     int op, tile, seg, kc;
-    ES_DEV void seek(const GvLaunch* L_, int s) {
+    __host__ __device__ void seek(const GvLaunch* L_, int s) {
         L = L_;
         op = 0;
         while (op + 1 < L->nops && L->ops[op + 1].stage0 <= s) ++op;
@@ -121,7 +121,7 @@ struct GvWalk {
     }
     // advance by n chunks within the current segment (n <= chunks left in
     // it); true when that finished the tile
-    ES_DEV bool advance(int n) {
+    __host__ __device__ bool advance(int n) {
         const GvOp& o = L->ops[op];
         kc += n;
         if (kc < L->segs[o.seg0 + seg].nck) return false;
@@ -481,6 +481,464 @@ gv_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __r
             __threadfence();
             post_rinv(L.post);
             if (threadIdx.x == 0) *done = 0;
+        }
+    }
+}
+
+// ------------------------------------------------------------ bf16: warp MMA
+// Tensor-core variant for bf16 weights (same descriptor; planned with
+// 128-row blocks and 128-column chunks).  Each warp of a CTA owns 16 rows of
+// the block -- the M side of mma.sync m16n8k16 -- and the (up to 8)
+// activation rows are its N side, so one MMA does the work of 256 fused
+// multiply-adds per activation row.
+//
+// Register-fed A operand.  In one k32 group lane (g = lane/4, c = lane%4)
+// loads 16 bytes of weight rows g and g+8 at columns 8c..8c+7: the fragments
+// of two k16 MMAs under a fixed permutation of k inside the group (a dot
+// product does not depend on the order of its terms).  MMA 0 takes columns
+// 8c+0..3 as its k = (2c, 2c+1, 2c+8, 2c+9), MMA 1 columns 8c+4..7.  The B
+// operand -- activation row g at the same eight columns -- is then one
+// 16-byte load as well.  Activations enter as two bf16 planes, hi = bf16(x)
+// and lo = bf16(x - hi), both multiplied into the same float32 accumulator,
+// so the products keep about 16 significant bits of x (float32-level
+// accuracy) at bf16 tensor-core cost.
+//
+// Work split: stream-K over CTA stages (op, 128-row block, segment,
+// 128-column chunk); all warps of a CTA walk the same stages, each over its
+// own 16 rows of the block, keeping GVM_D stages of weight loads in flight.
+// Blocks cut between CTAs are summed by the last CTA to arrive (partials in
+// CTA order: deterministic).
+// Activation windows: a CTA stages, as hi/lo planes in shared memory, only
+// the chunks of each source that its stage range multiplies (up to
+// GVM_NWIN windows while the budget lasts); anything else is read as
+// float32 through L2 and split in registers.  The planner sizes each
+// launch's shared memory to its largest window set: a larger request would
+// shrink the L1 that the streaming loads pass through.
+constexpr int GVM_ROWS = 16;                     // rows per warp
+constexpr int GVM_BLOCK = GVM_ROWS * GV_WARPS;   // rows per stage (128)
+constexpr int GVM_COLS = 128;                    // columns per stage
+constexpr int GVM_D = 2;                         // stages in flight per warp
+constexpr int GVM_NWIN = 16;                     // activation windows per CTA
+constexpr int GVM_PAD = 32;                      // plane padding (columns)
+constexpr int GVM_SCRATCH_CTAS = 1024;
+// partial sums [cta][cut][warp][set][lane x 4]
+constexpr int GVM_SCRATCH_FLOATS = GVM_SCRATCH_CTAS * 2 * GV_WARPS * 2 * 128;
+
+// chunks [klo, khi) of source src, hi/lo planes at word offset off of the
+// staged region (-1: read from global memory); plane width pw columns
+struct GvmWin { int src, klo, khi, off, pw, item0; };
+
+ES_DEV void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                           uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+ES_DEV uint32_t bf2_bits(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t*>(&v); }
+
+// hi/lo bf16 pairs of two floats (element 0 in the low half)
+ES_DEV void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float2 hf = __bfloat1622float2(h);
+    hi = bf2_bits(h);
+    lo = bf2_bits(__floats2bfloat162_rn(a - hf.x, b - hf.y));
+}
+
+// Four activations of source x, row m, columns k..k+3 (k + 3 < K): the raw
+// row plus `add`, normalised for XS_NORM.
+ES_DEV float4 gvm_x4(const GvXSrc& x, int m, int k) {
+    const size_t gi = (size_t)(m * x.row_stride + x.row_off) * x.ld + k;
+    float4 v = __ldcg(reinterpret_cast<const float4*>(x.src + gi));
+    if (x.add) {
+        const float4 a = __ldcg(reinterpret_cast<const float4*>(x.add + gi));
+        v.x += a.x; v.y += a.y; v.z += a.z; v.w += a.w;
+    }
+    if (x.kind == XS_NORM) {
+        const bf16* gp = (const bf16*)x.gain + k;
+        const float ri = __ldcg(x.rinv + m);
+        v.x *= ri * __bfloat162float(gp[0]);
+        v.y *= ri * __bfloat162float(gp[1]);
+        v.z *= ri * __bfloat162float(gp[2]);
+        v.w *= ri * __bfloat162float(gp[3]);
+    }
+    return v;
+}
+
+// The activation windows of CTA stage range [S0, S1) (one thread), staged
+// greedily in order while `budget` words of shared memory last.  Returns the
+// number of windows; *nitems = staging items (4 columns of one row) and
+// *used = words of the staged ones.  The planner runs the same function on
+// the host to size each launch's shared memory.
+__host__ __device__ inline int gvm_windows(const GvLaunch& L, int S0, int S1, GvmWin* win, int budget, int* nitems,
+                                           int* used_words) {
+    int n = 0;
+    GvWalk w;
+    w.seek(&L, S0);
+    for (int s = S0; s < S1;) {
+        const GvSeg& sg = L.segs[L.ops[w.op].seg0 + w.seg];
+        const int run = sg.nck - w.kc < S1 - s ? sg.nck - w.kc : S1 - s;
+        const int a = w.kc, b = w.kc + run;
+        int i = 0;
+        for (; i < n; ++i)
+            if (win[i].src == sg.xs && a <= win[i].khi && b >= win[i].klo) break;
+        if (i < n) {
+            if (a < win[i].klo) win[i].klo = a;
+            if (b > win[i].khi) win[i].khi = b;
+        } else if (n < GVM_NWIN) {
+            win[n].src = sg.xs; win[n].klo = a; win[n].khi = b;
+            ++n;
+        }
+        w.advance(run);
+        s += run;
+    }
+    // a widened window may now touch another of its source: merge those
+    for (bool again = true; again;) {
+        again = false;
+        for (int i = 0; i < n && !again; ++i)
+            for (int j = i + 1; j < n && !again; ++j)
+                if (win[i].src == win[j].src && win[j].klo <= win[i].khi && win[j].khi >= win[i].klo) {
+                    if (win[j].klo < win[i].klo) win[i].klo = win[j].klo;
+                    if (win[j].khi > win[i].khi) win[i].khi = win[j].khi;
+                    win[j] = win[--n];
+                    again = true;
+                }
+    }
+    int used = 0, items = 0;
+    for (int i = 0; i < n; ++i) {
+        const int cols = (win[i].khi - win[i].klo) * GVM_COLS;
+        win[i].pw = cols + GVM_PAD;
+        const int words = L.M * win[i].pw;
+        win[i].off = -1;
+        win[i].item0 = items;
+        if (used + words <= budget) {
+            win[i].off = used;
+            used += words;
+            items += L.M * (cols / 4);
+        }
+    }
+    *nitems = items;
+    *used_words = used;
+    return n;
+}
+
+// Stage the windows with off >= 0 as hi/lo planes (whole CTA; synchronises).
+ES_DEV void gvm_stage(const GvLaunch& L, const GvmWin* win, int nwin, int nitems, unsigned char* xsm) {
+    const int M = L.M;
+    constexpr int SB = 8;
+    for (int t0 = threadIdx.x; t0 < nitems; t0 += SB * GV_THREADS) {
+        float4 v[SB];
+        uint2* dh[SB];
+        int lo_off[SB];
+#pragma unroll
+        for (int u = 0; u < SB; ++u) {
+            const int t = t0 + u * GV_THREADS;
+            dh[u] = nullptr;
+            lo_off[u] = 0;
+            v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < nitems) {
+                int i = 0;
+                while (win[i].off < 0 || t >= win[i].item0 + M * ((win[i].khi - win[i].klo) * (GVM_COLS / 4))) ++i;
+                const GvmWin& wd = win[i];
+                const GvXSrc& x = L.xs[wd.src];
+                const int C4 = (wd.khi - wd.klo) * (GVM_COLS / 4), r = t - wd.item0, m = r / C4;
+                const int kr = (r - m * C4) * 4, k = wd.klo * GVM_COLS + kr;
+                if (k < x.K) v[u] = gvm_x4(x, m, k);
+                bf16* plane = reinterpret_cast<bf16*>(xsm + (size_t)wd.off * 4);
+                dh[u] = reinterpret_cast<uint2*>(plane + (size_t)m * wd.pw + kr);
+                lo_off[u] = M * wd.pw;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < SB; ++u) {
+            if (!dh[u]) continue;
+            uint2 h, l;
+            split2(v[u].x, v[u].y, h.x, l.x);
+            split2(v[u].z, v[u].w, h.y, l.y);
+            *dh[u] = h;
+            *reinterpret_cast<uint2*>(reinterpret_cast<bf16*>(dh[u]) + lo_off[u]) = l;
+        }
+    }
+    __syncthreads();
+}
+
+// weight fragments of one stage for this warp: rows g and g+8, four k32 groups
+struct GvmStage { uint4 a[4], b[4]; };
+
+// A run: chunks [kc, kc_end) of one segment of one tile.  The loops below
+// read the descriptor once per run, so a stage costs only its loads and MMAs.
+struct GvmRun { int op, tile, seg, kc, kc_end; };
+
+// Position (op, tile, segment, chunk) in the stage sequence of L.
+struct GvmPos { int op, tile, seg, kc; };
+
+ES_DEV GvmPos gvm_seek(const GvLaunch& L, int s) {
+    GvWalk w;
+    w.seek(&L, s);
+    return GvmPos{w.op, w.tile, w.seg, w.kc};
+}
+
+// The run starting at p, within stage range [.., s_end) (s: p's index);
+// p and s move past it.
+ES_DEV GvmRun gvm_next_run(const GvLaunch& L, GvmPos& p, int& s, int s_end) {
+    GvmRun r;
+    r.op = p.op; r.tile = p.tile; r.seg = p.seg; r.kc = p.kc;
+    const GvOp& o = L.ops[p.op];
+    const int nck = L.segs[o.seg0 + p.seg].nck;
+    const int n = min(nck - p.kc, s_end - s);
+    r.kc_end = p.kc + n;
+    s += n;
+    p.kc += n;
+    if (p.kc == nck) {
+        p.kc = 0;
+        if (++p.seg == o.nseg) {
+            p.seg = 0;
+            if (++p.tile == o.ntiles) { p.tile = 0; ++p.op; }
+        }
+    }
+    return r;
+}
+
+// Per-warp cursor state that only run boundaries touch (kept in shared
+// memory to leave the registers to the weight ring).  Every lane of the warp
+// writes the same values.
+struct GvmWarp {
+    GvmPos ip, cp;  // issue / consume positions after their current runs
+    int is, cs;     // their stage indices
+    int op, tile, src;  // the consume run's op, tile and activation source
+};
+
+// Issue side: this lane's weight row pointers in the current run.
+struct GvmIssue {
+    const bf16* ra;
+    const bf16* rb;
+    int K, kc, kc_end;
+};
+
+ES_DEV void gvm_issue_begin(const GvLaunch& L, GvmWarp& ws, GvmIssue& I, int s_end) {
+    const GvmRun r = gvm_next_run(L, ws.ip, ws.is, s_end);
+    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+    const GvOp& o = L.ops[r.op];
+    const GvSeg& sg = L.segs[o.seg0 + r.seg];
+    const int w0 = r.tile * GVM_BLOCK + (threadIdx.x >> 5) * GVM_ROWS;
+    // rows past N read the last row (their sums are dropped); warps wholly
+    // past N load nothing
+    I.ra = (const bf16*)sg.W + (size_t)min(w0 + g, o.N - 1) * sg.K + 8 * c;
+    I.rb = (const bf16*)sg.W + (size_t)min(w0 + g + 8, o.N - 1) * sg.K + 8 * c;
+    I.K = w0 < o.N ? sg.K - 8 * c : 0;  // this lane's columns start 8c further on
+    I.kc = r.kc;
+    I.kc_end = r.kc_end;
+}
+
+// Request chunk I.kc into st and step (a stage must remain in the range).
+ES_DEV void gvm_issue_step(const GvLaunch& L, GvmWarp& ws, GvmIssue& I, GvmStage& st, int s_end) {
+    const int kb = I.kc * GVM_COLS;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const bool in = kb + 32 * j < I.K;
+        st.a[j] = in ? ld_stream16(I.ra + kb + 32 * j) : make_uint4(0u, 0u, 0u, 0u);
+        st.b[j] = in ? ld_stream16(I.rb + kb + 32 * j) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (++I.kc == I.kc_end && ws.is < s_end) gvm_issue_begin(L, ws, I, s_end);
+}
+
+// Consume side: the activation operand of the current run.
+struct GvmCons {
+    int kc, kc_end, set;
+    bool tile_end;   // the run completes its tile
+    const bf16* ph;  // staged hi plane at this lane's row and column offset (null: global)
+    int lo;          // hi -> lo plane distance (elements)
+};
+
+ES_DEV void gvm_cons_begin(const GvLaunch& L, GvmWarp& ws, GvmCons& C, const GvmWin* win, int nwin,
+                           const unsigned char* xsm, int s_end) {
+    const GvmRun r = gvm_next_run(L, ws.cp, ws.cs, s_end);
+    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+    const GvOp& o = L.ops[r.op];
+    const GvSeg& sg = L.segs[o.seg0 + r.seg];
+    ws.op = r.op; ws.tile = r.tile; ws.src = sg.xs;
+    C.kc = r.kc; C.kc_end = r.kc_end;
+    C.set = sg.set;
+    C.tile_end = r.kc_end == sg.nck && r.seg == o.nseg - 1;
+    C.ph = nullptr;
+    C.lo = 0;
+    for (int i = 0; i < nwin; ++i)
+        if (win[i].src == sg.xs && r.kc >= win[i].klo && r.kc < win[i].khi) {
+            if (win[i].off >= 0) {
+                C.ph = reinterpret_cast<const bf16*>(xsm + (size_t)win[i].off * 4) + (size_t)g * win[i].pw -
+                       win[i].klo * GVM_COLS + 8 * c;
+                C.lo = L.M * win[i].pw;
+            }
+            break;
+        }
+}
+
+// B fragments (hi, lo) of group j of chunk C.kc read as float32 from
+// global memory: the fallback for sources without a staged window.
+ES_DEV void gvm_x_global(const GvLaunch& L, const GvmWarp& ws, const GvmCons& C, int j, uint4& bh, uint4& bl) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+    const GvXSrc& x = L.xs[ws.src];
+    const int k = C.kc * GVM_COLS + 32 * j + 8 * c;
+    bh = bl = make_uint4(0u, 0u, 0u, 0u);
+    if (g < L.M && k < x.K) {
+        const float4 f0 = gvm_x4(x, g, k), f1 = gvm_x4(x, g, k + 4);
+        split2(f0.x, f0.y, bh.x, bl.x);
+        split2(f0.z, f0.w, bh.y, bl.y);
+        split2(f1.x, f1.y, bh.z, bl.z);
+        split2(f1.z, f1.w, bh.w, bl.w);
+    }
+}
+
+// acc += W(chunk C.kc of this warp's rows) . x, and step.
+ES_DEV void gvm_cons_step(const GvLaunch& L, const GvmWarp& ws, GvmCons& C, const GvmStage& st, float (&acc)[4]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2;
+    const bool row_on = g < L.M;
+    const int kb = C.kc * GVM_COLS;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint4 bh = make_uint4(0u, 0u, 0u, 0u), bl = bh;
+        if (C.ph) {
+            if (row_on) {
+                bh = *reinterpret_cast<const uint4*>(C.ph + kb + 32 * j);
+                bl = *reinterpret_cast<const uint4*>(C.ph + C.lo + kb + 32 * j);
+            }
+        } else {
+            gvm_x_global(L, ws, C, j, bh, bl);
+        }
+        const uint4 a = st.a[j], b = st.b[j];
+        mma_bf16_16816(acc, a.x, b.x, a.y, b.y, bh.x, bh.y);
+        mma_bf16_16816(acc, a.z, b.z, a.w, b.w, bh.z, bh.w);
+        mma_bf16_16816(acc, a.x, b.x, a.y, b.y, bl.x, bl.y);
+        mma_bf16_16816(acc, a.z, b.z, a.w, b.w, bl.z, bl.w);
+    }
+    ++C.kc;
+}
+
+// Epilogue of one 16-row tile from the D fragments: lane (g, c) holds rows
+// (n0+g, n0+g+8) x activation rows (2c, 2c+1).
+ES_DEV void gvm_epilogue(const GvLaunch& L, const GvOp& o, int n0, const float (&v0)[4], const float (&v1)[4]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int m = 2 * c + (e & 1), n = n0 + g + (e >> 1) * 8;
+        if (m >= L.M || n >= o.N) continue;
+        float* y = o.y + (size_t)m * o.ldy + n;
+        switch (o.epi) {
+            case GEPI_STORE: *y = v0[e]; break;
+            case GEPI_ACC: *y = __ldcg(y) + v0[e]; break;
+            case GEPI_ACC_ADD: *y = __ldcg(y) + v0[e] + __ldcg(o.add + (size_t)m * o.ldy + n); break;
+            default: *y = silu_f(v0[e]) * v1[e]; break;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM)
+gvm_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __restrict__ counters,
+           int* __restrict__ done) {
+    extern __shared__ __align__(16) unsigned char gvm_xsm[];
+    __shared__ __align__(16) GvLaunch L;
+    __shared__ GvmWin win[GVM_NWIN];
+    __shared__ GvmWarp wstate[GV_WARPS];
+    __shared__ int s_nwin, s_items, s_last, s_done;
+    gv_load_desc(L, Lg);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int q = L.q, cta = blockIdx.x;
+    const int S0 = cta * q, S1 = min(L.nstages, S0 + q);
+    GvmWarp& ws = wstate[warp];
+    // nothing here depends on the previous kernel: the windows and the first
+    // GVM_D - 1 stages of weights are set up before waiting for it
+    if (tid == 0) {
+        int used;
+        s_nwin = gvm_windows(L, S0, S1, win, L.x_smem_floats, &s_items, &used);
+    }
+    GvmStage ring[GVM_D];
+    GvmIssue I;
+    int s_issue = S0;
+    ws.ip = ws.cp = gvm_seek(L, S0);
+    ws.is = ws.cs = S0;
+    gvm_issue_begin(L, ws, I, S1);
+#pragma unroll
+    for (int i = 0; i < GVM_D - 1; ++i)
+        if (s_issue < S1) { gvm_issue_step(L, ws, I, ring[i], S1); ++s_issue; }
+    __syncthreads();
+    grid_dep_wait();
+    grid_dep_launch();
+    const int nwin = s_nwin;
+    gvm_stage(L, win, nwin, s_items, gvm_xsm);
+
+    GvmCons C;
+    gvm_cons_begin(L, ws, C, win, nwin, gvm_xsm, S1);
+    float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+    int blk_first = S0 - (S0 - L.ops[ws.op].stage0) % L.ops[ws.op].spt;
+    for (int s = S0; s < S1; s += GVM_D) {
+#pragma unroll
+        for (int i = 0; i < GVM_D; ++i) {
+            const int si = s + i;
+            if (si >= S1) break;
+            if (s_issue < S1) {  // keep GVM_D - 1 stages ahead in flight
+                gvm_issue_step(L, ws, I, ring[(i + GVM_D - 1) % GVM_D], S1);
+                ++s_issue;
+            }
+            if (C.set == 0) gvm_cons_step(L, ws, C, ring[i], acc0);
+            else gvm_cons_step(L, ws, C, ring[i], acc1);
+            if (C.kc < C.kc_end) continue;
+            if (C.tile_end || si + 1 == S1) {
+                // ---- finish the block (or this CTA's part of it); CTA-uniform
+                const GvOp& o = L.ops[ws.op];
+                const bool two = o.epi == GEPI_SWIGLU;
+                const int blk_last = blk_first + o.spt - 1;
+                bool do_epi = blk_first >= S0 && blk_last < S1;
+                if (!do_epi) {
+                    const int sid = S0 >= blk_first ? 0 : 1;
+                    float* part = scratch + ((size_t)((cta * 2 + sid) * GV_WARPS + warp) * 2) * 128 + lane * 4;
+                    *reinterpret_cast<float4*>(part) = make_float4(acc0[0], acc0[1], acc0[2], acc0[3]);
+                    if (two) *reinterpret_cast<float4*>(part + 128) = make_float4(acc1[0], acc1[1], acc1[2], acc1[3]);
+                    __threadfence();
+                    __syncthreads();
+                    const int c_first = blk_first / q, c_last = blk_last / q;
+                    const int gblk = o.tile0 + ws.tile;
+                    if (tid == 0) s_last = atomicAdd(counters + gblk, 1) == c_last - c_first;
+                    __syncthreads();
+                    if (s_last) {
+                        __threadfence();
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc0[e] = acc1[e] = 0.f;
+                        for (int cc = c_first; cc <= c_last; ++cc) {
+                            const int sd = cc * q >= blk_first ? 0 : 1;
+                            const float* pp =
+                                scratch + ((size_t)((cc * 2 + sd) * GV_WARPS + warp) * 2) * 128 + lane * 4;
+                            const float4 p0 = __ldcg(reinterpret_cast<const float4*>(pp));
+                            acc0[0] += p0.x; acc0[1] += p0.y; acc0[2] += p0.z; acc0[3] += p0.w;
+                            if (two) {
+                                const float4 p1 = __ldcg(reinterpret_cast<const float4*>(pp + 128));
+                                acc1[0] += p1.x; acc1[1] += p1.y; acc1[2] += p1.z; acc1[3] += p1.w;
+                            }
+                        }
+                        if (tid == 0) counters[gblk] = 0;
+                        do_epi = true;
+                    }
+                    // every thread has read s_last before a later block changes it
+                    __syncthreads();
+                }
+                if (do_epi) gvm_epilogue(L, o, ws.tile * GVM_BLOCK + warp * GVM_ROWS, acc0, acc1);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc0[e] = acc1[e] = 0.f;
+                blk_first = blk_last + 1;
+            }
+            if (si + 1 < S1) gvm_cons_begin(L, ws, C, win, nwin, gvm_xsm, S1);
+        }
+    }
+    if (L.post.rows > 0) {
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) s_done = atomicAdd(done, 1) == (int)gridDim.x - 1;
+        __syncthreads();
+        if (s_done) {
+            __threadfence();
+            post_rinv(L.post);
+            if (tid == 0) *done = 0;
         }
     }
 }
