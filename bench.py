@@ -83,6 +83,26 @@ def phase_bytes(wl: dict, gamma: int, ctx: int) -> dict:
     return {"draft_fwd": draft_fwd, "draft": draft, "verify": verify}
 
 
+def measured_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary
+    (profiles/traffic.json), or None when there is none or the kernel source
+    has changed since the counters were taken (sha256 of its files)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    e = t.get(kernel)
+    if not e:
+        return None
+    h = hashlib.sha256()
+    for rel in e["sources"]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return e["dram_bytes_per_launch"] if h.hexdigest() == e["sources_sha256"] else None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -303,7 +323,7 @@ def run_ours(args, rank: int, world: int):
         "acceptance": {"tokens_per_phase": round(tok_per_phase, 3),
                        "rate": round(accepted / max(drafted, 1), 4)},
         "roofline": {"bound": "hbm", "kernel": name, "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": measured_traffic(name),
                      "launches": pn, "share_of_device_time": round(pms / total_prof_ms, 4),
                      "peak_source": peak_src},
         "clocks": clk, "gpu_launches": int(launches),

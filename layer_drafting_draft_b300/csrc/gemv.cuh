@@ -160,24 +160,50 @@ ES_DEV float warp_reduce_scatter(const float (&v)[NV], int lane) {
 }
 
 // ------------------------------------------------------------ post-norm
-// Executed by one whole CTA (blockDim.x a multiple of 32) once the rows it
-// reads are final: a warp per row.
+// Executed by one whole CTA (GV_THREADS threads) once the rows it reads are
+// final.  The CTA's threads stride over all rows at once so that every load
+// of every row is in flight together (one L2 round trip instead of one per
+// few columns), then reduce per row through shared memory.
 ES_DEV void post_rinv(const GvPost& p) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    for (int r = warp; r < p.rows; r += nw) {
-        const size_t base = (size_t)(r * p.row_stride + p.row_off) * p.K;
-        float ss = 0.f;
-#pragma unroll 4
-        for (int k = lane * 4; k < p.K; k += 128) {
-            float4 v = __ldcg(reinterpret_cast<const float4*>(p.h + base + k));
-            if (p.add) {
-                const float4 a = __ldcg(reinterpret_cast<const float4*>(p.add + base + k));
-                v.x += a.x; v.y += a.y; v.z += a.z; v.w += a.w;
+    constexpr int ROWS = GV_MAXM, NW = GV_THREADS / 32;
+    __shared__ float red[NW][ROWS];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int K4 = p.K >> 2;
+    for (int r0 = 0; r0 < p.rows; r0 += ROWS) {
+        const int nr = min(ROWS, p.rows - r0);
+        float ss[ROWS];
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) ss[r] = 0.f;
+        for (int k4 = tid; k4 < K4; k4 += GV_THREADS) {
+            float4 v[ROWS];
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) {
+                v[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (r < nr) {
+                    const size_t base = (size_t)((r0 + r) * p.row_stride + p.row_off) * p.K + 4 * k4;
+                    v[r] = __ldcg(reinterpret_cast<const float4*>(p.h + base));
+                    if (p.add) {
+                        const float4 a = __ldcg(reinterpret_cast<const float4*>(p.add + base));
+                        v[r].x += a.x; v[r].y += a.y; v[r].z += a.z; v[r].w += a.w;
+                    }
+                }
             }
-            ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r)
+                ss[r] += v[r].x * v[r].x + v[r].y * v[r].y + v[r].z * v[r].z + v[r].w * v[r].w;
         }
-        ss = warp_sum(ss);
-        if (lane == 0) p.rinv[r] = 1.0f / sqrtf(ss / (float)p.K + p.eps);
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            const float t = warp_sum(ss[r]);
+            if (lane == 0) red[warp][r] = t;
+        }
+        __syncthreads();
+        if (tid < nr) {
+            float t = 0.f;
+            for (int w = 0; w < NW; ++w) t += red[w][tid];
+            p.rinv[r0 + tid] = 1.0f / sqrtf(t / (float)p.K + p.eps);
+        }
+        __syncthreads();
     }
 }
 
@@ -712,9 +738,10 @@ struct GvmWarp {
 
 // Issue side: this lane's weight row pointers in the current run.
 struct GvmIssue {
-    const bf16* ra;
-    const bf16* rb;
-    int K, kc, kc_end;
+    const bf16* ra;  // row g, from column 8c
+    const bf16* rb;  // row g + 8, from column 8c
+    int K;           // segment width (0 for a warp wholly past N)
+    int kc, kc_end;
 };
 
 ES_DEV void gvm_issue_begin(const GvLaunch& L, GvmWarp& ws, GvmIssue& I, int s_end) {
@@ -727,19 +754,33 @@ ES_DEV void gvm_issue_begin(const GvLaunch& L, GvmWarp& ws, GvmIssue& I, int s_e
     // past N load nothing
     I.ra = (const bf16*)sg.W + (size_t)min(w0 + g, o.N - 1) * sg.K + 8 * c;
     I.rb = (const bf16*)sg.W + (size_t)min(w0 + g + 8, o.N - 1) * sg.K + 8 * c;
-    I.K = w0 < o.N ? sg.K - 8 * c : 0;  // this lane's columns start 8c further on
+    I.K = w0 < o.N ? sg.K : 0;
     I.kc = r.kc;
     I.kc_end = r.kc_end;
 }
 
 // Request chunk I.kc into st and step (a stage must remain in the range).
+// Whole chunks take unpredicated loads; only a segment's ragged last chunk
+// (or a warp past N) checks columns.  (A bulk L2 prefetch of the chunk 4 or
+// 8 stages ahead measured slower: 223 and 219 against 236 tok/s.)
 ES_DEV void gvm_issue_step(const GvLaunch& L, GvmWarp& ws, GvmIssue& I, GvmStage& st, int s_end) {
     const int kb = I.kc * GVM_COLS;
+    const bf16* pa = I.ra + kb;
+    const bf16* pb = I.rb + kb;
+    if (kb + GVM_COLS <= I.K) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const bool in = kb + 32 * j < I.K;
-        st.a[j] = in ? ld_stream16(I.ra + kb + 32 * j) : make_uint4(0u, 0u, 0u, 0u);
-        st.b[j] = in ? ld_stream16(I.rb + kb + 32 * j) : make_uint4(0u, 0u, 0u, 0u);
+        for (int j = 0; j < 4; ++j) {
+            st.a[j] = ld_stream16(pa + 32 * j);
+            st.b[j] = ld_stream16(pb + 32 * j);
+        }
+    } else {
+        const int kl = I.K - 8 * (threadIdx.x & 3) - kb;  // this lane's columns left in the segment
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const bool in = 32 * j < kl;
+            st.a[j] = in ? ld_stream16(pa + 32 * j) : make_uint4(0u, 0u, 0u, 0u);
+            st.b[j] = in ? ld_stream16(pb + 32 * j) : make_uint4(0u, 0u, 0u, 0u);
+        }
     }
     if (++I.kc == I.kc_end && ws.is < s_end) gvm_issue_begin(L, ws, I, s_end);
 }
@@ -747,9 +788,11 @@ ES_DEV void gvm_issue_step(const GvLaunch& L, GvmWarp& ws, GvmIssue& I, GvmStage
 // Consume side: the activation operand of the current run.
 struct GvmCons {
     int kc, kc_end, set;
-    bool tile_end;   // the run completes its tile
-    const bf16* ph;  // staged hi plane at this lane's row and column offset (null: global)
-    int lo;          // hi -> lo plane distance (elements)
+    bool tile_end;  // the run completes its tile
+    bool glob;      // no staged window: read float32 through L2
+    uint32_t sa;    // shared address of this lane's hi-plane fragment at column 0 of the window
+    uint32_t lo;    // hi -> lo plane distance (bytes)
+    int kbase;      // first column of the window
 };
 
 ES_DEV void gvm_cons_begin(const GvLaunch& L, GvmWarp& ws, GvmCons& C, const GvmWin* win, int nwin,
@@ -762,17 +805,28 @@ ES_DEV void gvm_cons_begin(const GvLaunch& L, GvmWarp& ws, GvmCons& C, const Gvm
     C.kc = r.kc; C.kc_end = r.kc_end;
     C.set = sg.set;
     C.tile_end = r.kc_end == sg.nck && r.seg == o.nseg - 1;
-    C.ph = nullptr;
-    C.lo = 0;
+    C.glob = true;
+    C.sa = 0; C.lo = 0; C.kbase = 0;
     for (int i = 0; i < nwin; ++i)
         if (win[i].src == sg.xs && r.kc >= win[i].klo && r.kc < win[i].khi) {
             if (win[i].off >= 0) {
-                C.ph = reinterpret_cast<const bf16*>(xsm + (size_t)win[i].off * 4) + (size_t)g * win[i].pw -
-                       win[i].klo * GVM_COLS + 8 * c;
-                C.lo = L.M * win[i].pw;
+                // lanes of activation rows >= M read row M-1: the MMA columns
+                // they feed are never stored
+                const int row = min(g, L.M - 1);
+                C.glob = false;
+                C.sa = (uint32_t)__cvta_generic_to_shared(xsm) + (uint32_t)win[i].off * 4u +
+                       (uint32_t)(row * win[i].pw + 8 * c) * 2u;
+                C.lo = (uint32_t)(L.M * win[i].pw) * 2u;
+                C.kbase = win[i].klo * GVM_COLS;
             }
             break;
         }
+}
+
+ES_DEV uint4 lds16(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
 }
 
 // B fragments (hi, lo) of group j of chunk C.kc read as float32 from
@@ -791,27 +845,32 @@ ES_DEV void gvm_x_global(const GvLaunch& L, const GvmWarp& ws, const GvmCons& C,
     }
 }
 
+ES_DEV void gvm_mma_group(float (&acc)[4], const uint4& a, const uint4& b, const uint4& bh, const uint4& bl) {
+    mma_bf16_16816(acc, a.x, b.x, a.y, b.y, bh.x, bh.y);
+    mma_bf16_16816(acc, a.z, b.z, a.w, b.w, bh.z, bh.w);
+    mma_bf16_16816(acc, a.x, b.x, a.y, b.y, bl.x, bl.y);
+    mma_bf16_16816(acc, a.z, b.z, a.w, b.w, bl.z, bl.w);
+}
+
 // acc += W(chunk C.kc of this warp's rows) . x, and step.
 ES_DEV void gvm_cons_step(const GvLaunch& L, const GvmWarp& ws, GvmCons& C, const GvmStage& st, float (&acc)[4]) {
-    const int lane = threadIdx.x & 31, g = lane >> 2;
-    const bool row_on = g < L.M;
-    const int kb = C.kc * GVM_COLS;
+    if (!C.glob) {
+        const uint32_t a0 = C.sa + (uint32_t)(C.kc * GVM_COLS - C.kbase) * 2u;
+        uint4 bh[4], bl[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        uint4 bh = make_uint4(0u, 0u, 0u, 0u), bl = bh;
-        if (C.ph) {
-            if (row_on) {
-                bh = *reinterpret_cast<const uint4*>(C.ph + kb + 32 * j);
-                bl = *reinterpret_cast<const uint4*>(C.ph + C.lo + kb + 32 * j);
-            }
-        } else {
-            gvm_x_global(L, ws, C, j, bh, bl);
+        for (int j = 0; j < 4; ++j) {
+            bh[j] = lds16(a0 + 64 * j);
+            bl[j] = lds16(a0 + C.lo + 64 * j);
         }
-        const uint4 a = st.a[j], b = st.b[j];
-        mma_bf16_16816(acc, a.x, b.x, a.y, b.y, bh.x, bh.y);
-        mma_bf16_16816(acc, a.z, b.z, a.w, b.w, bh.z, bh.w);
-        mma_bf16_16816(acc, a.x, b.x, a.y, b.y, bl.x, bl.y);
-        mma_bf16_16816(acc, a.z, b.z, a.w, b.w, bl.z, bl.w);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) gvm_mma_group(acc, st.a[j], st.b[j], bh[j], bl[j]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint4 bh, bl;
+            gvm_x_global(L, ws, C, j, bh, bl);
+            gvm_mma_group(acc, st.a[j], st.b[j], bh, bl);
+        }
     }
     ++C.kc;
 }
