@@ -12,9 +12,12 @@ temperature 1.0), random-initialised weights and uniform prompt ids.
   e2e        the same generation through the C-ABI call generate() with host
              buffers: prompt upload, both prefills, decoding and the token
              read-back inside the timed region (host wall clock)
-  draft/verify  per-phase breakdown (CUDA events around draft_step and
-             verify_step) and their fraction of the HBM weight-stream
-             roofline: bytes = weights streamed + KV read/written
+  draft/verify  per-phase breakdown of one more generation (the library's
+             part timing: CUDA events around each phase part's graph
+             launch): calibration, the gamma-1 fuzzy drafts ("fuzzy": the
+             layer-parallel draft forwards alone) and verify+accept, each
+             with its fraction of the HBM weight-stream roofline: bytes =
+             weights streamed + KV read/written
   roofline   the dominant kernel (most device time in a per-launch event
              pass over one generation): algorithmic bytes / event time vs the
              measured HBM copy bandwidth
@@ -55,7 +58,8 @@ def parse():
     ap.add_argument("--mode", default="full", choices=["full", "attn"])
     ap.add_argument("--temperature", type=float, default=1.0)
     ap.add_argument("--gamma", type=int, default=None)
-    ap.add_argument("--breakdown-phases", type=int, default=8)
+    ap.add_argument("--sigma", type=float, default=None,
+                    help="self-draft workloads: draft = base + N(0, (sigma*0.02)^2)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -74,13 +78,20 @@ def kv_bytes(s: dict, esz: int, ctx: int, rows: int) -> float:
     return per_pos * (ctx * rows + rows)
 
 
+def shape_str(s: dict) -> str:
+    return (f"{s['n_layers']}L d{s['d']} {s['n_heads']}H/{s['n_kv_heads']}KV hd{s['head_dim']} "
+            f"ffn{s['ffn']} V{s['vocab']}")
+
+
 def phase_bytes(wl: dict, gamma: int, ctx: int) -> dict:
     esz = 2 if wl["dtype"] == "bf16" else 4
     wd, wb = weight_bytes(wl["draft"], esz), weight_bytes(wl["base"], esz)
     draft_fwd = wd["layers"] + wd["head"] + wd["embed_row"]
     draft = gamma * draft_fwd + kv_bytes(wl["draft"], esz, ctx, 2 * gamma)
+    # the gamma - 1 fuzzy forwards alone (one row each)
+    fuzzy = (gamma - 1) * draft_fwd + kv_bytes(wl["draft"], esz, ctx, gamma - 1)
     verify = wb["layers"] + wb["head"] + (gamma + 1) * wb["embed_row"] + kv_bytes(wl["base"], esz, ctx, gamma + 1)
-    return {"draft_fwd": draft_fwd, "draft": draft, "verify": verify}
+    return {"draft_fwd": draft_fwd, "draft": draft, "fuzzy": fuzzy, "verify": verify}
 
 
 def measured_traffic(kernel: str):
@@ -212,7 +223,7 @@ def run_ours(args, rank: int, world: int):
     wl = synth.WORKLOADS[args.workload]
     gamma = args.gamma or wl["gamma"]
     P, max_new, T, k = wl["prompt"], wl["max_new"], args.temperature, args.k
-    draft_w, base_w, prompts = synth.make_pair(args.workload, device="cuda")
+    draft_w, base_w, prompts = synth.make_pair(args.workload, device="cuda", sigma=args.sigma)
     prompts = prompts[:1].numpy() if wl["batch"] >= 1 else prompts.numpy()
     stream = torch.cuda.Stream()
     mode = ES_FULL_LAYER if args.mode == "full" else ES_ATTN_ONLY
@@ -256,24 +267,23 @@ def run_ours(args, rank: int, world: int):
     launches = sum(s["kernel_launches"] for s in stats)
     tok_per_phase = emitted / max(phases, 1)
 
-    # ---- per-phase breakdown (draft part / verify part), CUDA events
+    # ---- per-phase breakdown: one more generation with the library's part
+    # timing (CUDA events around each phase part's graph launch, calibration
+    # and fuzzy drafts as two graphs)
     g.easyspec_prefill(prompts)
-    d_ms, v_ms = [], []
-    for i in range(args.breakdown_phases):
-        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-        e0.record(stream)
-        g.draft_step(k, gamma, T, 77 + i)
-        e1.record(stream)
-        g.verify_step(T, 77 + i, gamma)
-        e2.record(stream)
-        e2.synchronize()
-        if i > 0:
-            d_ms.append(e0.elapsed_time(e1))
-            v_ms.append(e1.elapsed_time(e2))
+    g.es_profile(2)
+    st_parts = g.es_decode(max_new, gamma, k, T, seed0 + 777)
+    parts = g.es_profile_read()
+    g.es_profile(0)
+    nph = max(st_parts["phases"], 1)
+    calib_ms = parts["phase.calibrate"][0] / nph
+    fuzzy_ms = parts["phase.fuzzy"][0] / nph
+    verify_ms = parts["phase.verify"][0] / nph
+    draft_ms = calib_ms + fuzzy_ms
     peak, peak_src = peaks()
     pb = phase_bytes(wl, gamma, P + max_new // 2)
-    draft_ms, verify_ms = statistics.median(d_ms), statistics.median(v_ms)
     draft_gbs = pb["draft"] / (draft_ms * 1e-3) / 1e9
+    fuzzy_gbs = pb["fuzzy"] / (fuzzy_ms * 1e-3) / 1e9
     verify_gbs = pb["verify"] / (verify_ms * 1e-3) / 1e9
     phase_roof_s = (pb["draft"] + pb["verify"]) / (peak * 1e9)
     roof_tok_s = tok_per_phase / phase_roof_s
@@ -305,17 +315,22 @@ def run_ours(args, rank: int, world: int):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total_ms / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl["dtype"], "data": "synthetic",
-        "config": {"workload": args.workload, "draft": "24L d896 14H/2KV ffn4864 V151936",
-                   "base": "28L d3584 28H/4KV ffn18944 V151936", "batch": 1, "prompt": P,
-                   "max_new": max_new, "gamma": gamma, "k": k, "mode": args.mode,
-                   "temperature": T, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (weights 16.5 GB streamed per phase)"},
+        "config": {"workload": args.workload, "draft": shape_str(wl["draft"]), "base": shape_str(wl["base"]),
+                   "batch": 1, "prompt": P, "max_new": max_new, "gamma": gamma, "k": k, "mode": args.mode,
+                   "temperature": T, "sigma": args.sigma, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2 (weights {(pb['draft'] + pb['verify']) / 1e9:.1f} GB "
+                         f"streamed per phase)"},
         "e2e": {"value": round(e2e_value, 2), "unit": "tok/s",
                 "h2d_bytes_per_step": int(prompts.size * 4 + 16 + 8),
                 "d2h_bytes_per_step": int(max_new * 4)},
         "draft": {"tok_s": round(gamma / (draft_ms * 1e-3), 1), "ms_per_phase": round(draft_ms, 4),
                   "achieved_gbs": round(draft_gbs, 1), "roofline_frac": round(draft_gbs / peak, 4),
-                  "bytes_per_phase": int(pb["draft"])},
+                  "bytes_per_phase": int(pb["draft"]),
+                  "calibrate_ms_per_phase": round(calib_ms, 4),
+                  "fuzzy": {"tok_s": round((gamma - 1) / (fuzzy_ms * 1e-3), 1),
+                            "ms_per_phase": round(fuzzy_ms, 4), "achieved_gbs": round(fuzzy_gbs, 1),
+                            "roofline_frac": round(fuzzy_gbs / peak, 4),
+                            "bytes_per_phase": int(pb["fuzzy"])}},
         "verify": {"ms_per_phase": round(verify_ms, 4), "achieved_gbs": round(verify_gbs, 1),
                    "roofline_frac": round(verify_gbs / peak, 4), "bytes_per_phase": int(pb["verify"])},
         "weight_stream_roofline": {"tok_s": round(roof_tok_s, 1), "e2e_frac": round(value / world / roof_tok_s, 4),

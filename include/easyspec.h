@@ -177,12 +177,17 @@ ES_API es_status generate(es_ctx *ctx, const int32_t *prompts, int B, int P,
 ES_API es_status es_decode(es_ctx *ctx, int max_new, int gamma, int k, float temperature,
                            uint64_t seed, es_stats *stats);
 
-/* Per-kernel timing for measurement: with on != 0 every later launch runs
- * outside CUDA graphs, bracketed by CUDA events on the context's stream;
- * es_profile_read() then reports, per kernel name (entries idx = 0, 1, ...
- * until ES_ERR_ARG), the summed event time in ms, the launch count and the
+/* Timing for measurement.  on = 1 (per kernel): every later launch runs
+ * outside CUDA graphs, bracketed by CUDA events on the context's stream, and
+ * is reported under "<model>.<step>" labels.  on = 2 (per phase part): the
+ * CUDA graphs stay; each graph launch is bracketed by events ("phase.draft",
+ * "phase.verify", "phase.calibrate", "phase.fuzzy"; es_decode then launches
+ * calibration and the fuzzy drafts as two graphs).  on = 0: off.
+ * es_profile_read() reports, per label (entries idx = 0, 1, ... until
+ * ES_ERR_ARG), the summed event time in ms, the launch count and the
  * algorithmic bytes of those launches (weights plus activations moved; 0 for
- * kernels whose traffic is not modelled).  es_profile() resets the totals. */
+ * kernels whose traffic is not modelled and for parts).  es_profile() resets
+ * the totals; another `on` is ES_ERR_ARG. */
 ES_API es_status es_profile(es_ctx *ctx, int on);
 ES_API es_status es_profile_read(es_ctx *ctx, int idx, char *name, int name_cap, double *ms,
                                  int64_t *launches, double *bytes);

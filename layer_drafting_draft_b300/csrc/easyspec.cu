@@ -137,7 +137,8 @@ struct es_ctx {
 
     // launch accounting and optional per-launch event timing
     int64_t launches = 0;
-    bool profiling = false;
+    bool profiling = false;   // per-kernel timing: eager launches bracketed by events
+    bool part_timing = false;  // per-part timing: graph launches bracketed by events
     std::vector<ProfRec> prof_pending;
     std::vector<std::pair<cudaEvent_t, cudaEvent_t>> prof_pool;
     size_t prof_pool_used = 0;
@@ -887,7 +888,22 @@ void run_part(es_ctx* c, int part, int gamma, int k) {
         CK(cudaGraphDestroy(g));
         it = c->graphs.emplace(key, gr).first;
     }
-    CK(cudaGraphLaunch(it->second.exec, c->st));
+    if (c->part_timing) {
+        static const char* const names[4] = {"phase.draft", "phase.verify", "phase.calibrate", "phase.fuzzy"};
+        if (c->prof_pool_used == c->prof_pool.size()) {
+            cudaEvent_t x, y;
+            CK(cudaEventCreate(&x));
+            CK(cudaEventCreate(&y));
+            c->prof_pool.emplace_back(x, y);
+        }
+        const auto ev = c->prof_pool[c->prof_pool_used++];
+        CK(cudaEventRecord(ev.first, c->st));
+        CK(cudaGraphLaunch(it->second.exec, c->st));
+        CK(cudaEventRecord(ev.second, c->st));
+        c->prof_pending.push_back(ProfRec{names[part], 0.0, ev.first, ev.second});
+    } else {
+        CK(cudaGraphLaunch(it->second.exec, c->st));
+    }
     c->launches += it->second.kernels;
 }
 
@@ -999,7 +1015,12 @@ es_stats do_decode(es_ctx* c, int max_new, int gamma, int k, float temperature, 
         if (rem <= 0) break;
         const int nph = (rem + gamma) / (gamma + 1);
         for (int i = 0; i < nph; ++i) {
-            run_part(c, 0, gamma, kk);
+            if (c->part_timing) {  // the same kernels as part 0, timed as two graphs
+                run_part(c, 2, gamma, 1);
+                run_part(c, 3, gamma, kk);
+            } else {
+                run_part(c, 0, gamma, kk);
+            }
             run_part(c, 1, gamma, kk);
         }
         s.phases += nph;
@@ -1251,8 +1272,10 @@ es_status es_profile(es_ctx* c, int on) {
     if (!c) return ES_ERR_ARG;
     return guarded(c, [&] {
         CK(cudaStreamSynchronize(c->st));
-        if (c->profiling) prof_collect(c);
-        c->profiling = on != 0;
+        if (c->profiling || c->part_timing) prof_collect(c);
+        if (on < 0 || on > 2) arg_fail(ES_ERR_ARG, "es_profile: mode %d (0, 1 or 2)", on);
+        c->profiling = on == 1;
+        c->part_timing = on == 2;
         c->prof.clear();
     });
 }
@@ -1261,7 +1284,7 @@ es_status es_profile_read(es_ctx* c, int idx, char* name, int name_cap, double* 
                           int64_t* launches, double* bytes) {
     if (!c || !name || name_cap < 1) return ES_ERR_ARG;
     return guarded(c, [&] {
-        if (c->profiling) {
+        if (c->profiling || c->part_timing) {
             CK(cudaStreamSynchronize(c->st));
             prof_collect(c);
         }

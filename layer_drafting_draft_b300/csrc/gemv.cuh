@@ -964,15 +964,33 @@ gvm_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __
                         __threadfence();
 #pragma unroll
                         for (int e = 0; e < 4; ++e) acc0[e] = acc1[e] = 0.f;
-                        for (int cc = c_first; cc <= c_last; ++cc) {
-                            const int sd = cc * q >= blk_first ? 0 : 1;
-                            const float* pp =
-                                scratch + ((size_t)((cc * 2 + sd) * GV_WARPS + warp) * 2) * 128 + lane * 4;
-                            const float4 p0 = __ldcg(reinterpret_cast<const float4*>(pp));
-                            acc0[0] += p0.x; acc0[1] += p0.y; acc0[2] += p0.z; acc0[3] += p0.w;
-                            if (two) {
-                                const float4 p1 = __ldcg(reinterpret_cast<const float4*>(pp + 128));
-                                acc1[0] += p1.x; acc1[1] += p1.y; acc1[2] += p1.z; acc1[3] += p1.w;
+                        // partials of CTAs c_first..c_last, summed in CTA order;
+                        // the loads of a batch are all in flight together
+                        constexpr int RB = 8;
+                        for (int set = 0; set < (two ? 2 : 1); ++set) {
+                            float v[4] = {0.f, 0.f, 0.f, 0.f};
+                            for (int cb = c_first; cb <= c_last; cb += RB) {
+                                float4 pv[RB];
+#pragma unroll
+                                for (int u = 0; u < RB; ++u) {
+                                    const int cc = cb + u;
+                                    pv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                                    if (cc <= c_last) {
+                                        const int sd = cc * q >= blk_first ? 0 : 1;
+                                        pv[u] = __ldcg(reinterpret_cast<const float4*>(
+                                            scratch + ((size_t)((cc * 2 + sd) * GV_WARPS + warp) * 2 + set) * 128 +
+                                            lane * 4));
+                                    }
+                                }
+#pragma unroll
+                                for (int u = 0; u < RB; ++u) {
+                                    v[0] += pv[u].x; v[1] += pv[u].y; v[2] += pv[u].z; v[3] += pv[u].w;
+                                }
+                            }
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                if (set == 0) acc0[e] = v[e];
+                                else acc1[e] = v[e];
                             }
                         }
                         if (tid == 0) counters[gblk] = 0;

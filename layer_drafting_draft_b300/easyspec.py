@@ -215,8 +215,9 @@ class EasySpec:
         self._check(self._lib.es_decode(self.ctx, max_new, gamma, k, temperature, seed, C.byref(st)))
         return {f: getattr(st, f) for f, _ in es_stats._fields_}
 
-    def es_profile(self, on: bool):
-        self._check(self._lib.es_profile(self.ctx, 1 if on else 0))
+    def es_profile(self, on):
+        """on: False/0 off, True/1 per kernel, 2 per phase part (graphs kept)."""
+        self._check(self._lib.es_profile(self.ctx, int(on)))
 
     def es_profile_read(self):
         """{kernel name: (ms, launches, algorithmic bytes)} since es_profile()."""
