@@ -79,6 +79,7 @@ struct Model {
     std::vector<Layer> ly;
     KVGeom g{};
     float* rope = nullptr;
+    float* ssp = nullptr;  // sums of squares for the next normalisation (bf16 fast path)
     int slots = 1, Mw = 0, nsplit = 0;
     float *h = nullptr, *xf = nullptr, *part = nullptr, *rinv = nullptr;
     std::vector<float*> xb, mb, q, k, v, a, s, A;
@@ -284,6 +285,9 @@ void setup_model(es_ctx* c, Model& m, const es_model_shape& s, const es_weights*
     m.h = c->dalloc<float>(Mw * m.d);
     m.xf = c->dalloc<float>(Mw * m.d);
     m.rinv = c->dalloc<float>(Mw);
+    // sums of squares per 16-column tile of h (tensor-core launches); a
+    // 128-row block may end up to 7 tiles past d
+    m.ssp = c->dalloc<float>((size_t)((m.d + GVM_ROWS - 1) / GVM_ROWS + 8) * Mw);
     for (int j = 0; j < slots; ++j) {
         m.xb.push_back(c->dalloc<float>(Mw * m.d));
         m.mb.push_back(c->dalloc<float>(Mw * m.d));
@@ -363,6 +367,14 @@ struct GvBuild {
         if (o.nseg >= GV_MAX_SEG || nsegs >= GV_MAX_SEGS) arg_fail(ES_ERR_ARG, "too many K-concatenated segments");
         if (xs < 0 || L->xs[xs].K != K) arg_fail(ES_ERR_ARG, "segment / source width mismatch");
         if (mma && K % 8) arg_fail(ES_ERR_ARG, "bf16 weight rows must be a multiple of 8 elements (K = %d)", K);
+        // an op's sums are scaled by the row's 1/rms when its sources are
+        // normalised: all of its segments must then read normalised sources
+        if (mma && o.nseg > 0) {
+            const GvXSrc& x0 = L->xs[L->segs[o.seg0].xs];
+            const GvXSrc& x1 = L->xs[xs];
+            if ((x0.kind == XS_NORM) != (x1.kind == XS_NORM) || x0.rinv != x1.rinv)
+                arg_fail(ES_ERR_ARG, "internal: an op mixes normalised and raw sources");
+        }
         GvSeg& s = L->segs[nsegs];
         s.W = W; s.K = K; s.xs = xs; s.set = set;
         o.nseg++;
@@ -499,11 +511,21 @@ Plan build_forward(es_ctx* c, Model& m, const std::vector<std::vector<int>>& gro
     int writer = -1;  // index in P.recs of the last weight launch (-1: embedding)
     // 1/rms of the rows the next launch normalises, computed at the end of
     // the launch before it
+    // Tensor-core launches (bf16) pass sums of squares instead: the writer's
+    // epilogue stores one partial per 16-column tile (the embedding kernel
+    // one per row) and the consumer adds them while it stages.
+    const bool ss_mode = fast && m.esz == 2;
+    int ss_tiles = 0;
     auto request = [&](const float* add, int rows, int stride, int off) {
         GvPost& p = writer < 0 ? P.first : P.recs[writer].host->post;
         if (p.rows) arg_fail(ES_ERR_ARG, "internal: two normalisations after one launch");
         p.h = m.h; p.add = add; p.rinv = m.rinv; p.rows = rows; p.row_stride = stride; p.row_off = off;
         p.K = m.d; p.eps = m.eps;
+        if (ss_mode) {
+            p.ssp = m.ssp;
+            p.op = 0;  // the writer's op 0 produces h (or, for attention-only sets, A_0)
+            ss_tiles = writer < 0 ? 1 : (m.d + GVM_ROWS - 1) / GVM_ROWS;
+        }
     };
     // a normalised input of the launch being built: fused into its staging
     // when it fits, else written beforehand by a norm launch (which also
@@ -511,8 +533,15 @@ Plan build_forward(es_ctx* c, Model& m, const std::vector<std::vector<int>>& gro
     auto norm_input = [&](GvBuild& b, NormArgs& pre, const void* gain, float* buf, const float* add,
                           int rs, int ro, bool* fused) -> int {
         if (fast) {
-            const int xs = b.norm_source(m.h, add, gain, m.rinv, m.d, rs, ro);
-            if (xs >= 0) { if (fused) *fused = true; return xs; }
+            const int xs = b.norm_source(m.h, add, gain, ss_mode ? m.ssp : m.rinv, m.d, rs, ro);
+            if (xs >= 0) {
+                if (ss_mode) {
+                    GvXSrc& x = b.L->xs[xs];
+                    x.ss_tiles = ss_tiles; x.ss_ld = M; x.eps = m.eps;
+                }
+                if (fused) *fused = true;
+                return xs;
+            }
         }
         if (fused) *fused = false;
         pre.add = add; pre.src_stride = rs; pre.src_off = ro;

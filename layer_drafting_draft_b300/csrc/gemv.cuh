@@ -74,6 +74,12 @@ struct GvXSrc {
     int smem_off;  // float offset in the staged region, or -1: read from global
     int item0;     // first staging item (4 columns of one row) of this source
     int pad_;
+    // XS_NORM with ss_tiles > 0 (tensor-core kernel): `rinv` holds the
+    // producing launch's sums of squares instead, ss_tiles partials per row
+    // at rinv[t * ss_ld + row]; the consumer adds them and takes 1/rms.
+    int ss_tiles, ss_ld;
+    float eps;
+    int pad2_;
 };
 struct GvSeg { const void* W; int K, xs, set, nck; };
 struct GvOp {
@@ -89,6 +95,11 @@ struct GvPost {
     const float* h; const float* add; float* rinv;
     int rows, row_stride, row_off, K;
     float eps; int pad_;
+    // tensor-core kernel: instead of a last-CTA pass, the epilogue of op
+    // `op` stores sums of squares of (h + add) over each of its 16-column
+    // tiles: ssp[tile * M + row] (M = the launch's rows)
+    float* ssp;
+    int op, pad2_;
 };
 struct GvLaunch {
     int nops, nxs, M, ntiles, nstages, q, x_smem_floats, ntiles64, x_items, pad_;
@@ -157,6 +168,19 @@ ES_DEV float warp_reduce_scatter(const float (&v)[NV], int lane) {
         }
     }
     return a[0];
+}
+
+// Arrival of a whole CTA at a counter shared by several CTAs: after the
+// barrier, one release-acquire atomic by thread 0 publishes every thread's
+// earlier writes (the barrier orders them before the release) and, for the
+// last arriver, makes the other CTAs' writes visible to it (its threads read
+// them after the barrier that follows).  Returns the counter's old value to
+// thread 0 (undefined elsewhere).
+ES_DEV int cta_arrive(int* ctr) {
+    int old = 0;
+    if (threadIdx.x == 0)
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(ctr) : "memory");
+    return old;
 }
 
 // ------------------------------------------------------------ post-norm
@@ -575,7 +599,7 @@ ES_DEV void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
 
 // Four activations of source x, row m, columns k..k+3 (k + 3 < K): the raw
 // row plus `add`, normalised for XS_NORM.
-ES_DEV float4 gvm_x4(const GvXSrc& x, int m, int k) {
+ES_DEV float4 gvm_x4(const GvXSrc& x, int m, int k, const float* srinv) {
     const size_t gi = (size_t)(m * x.row_stride + x.row_off) * x.ld + k;
     float4 v = __ldcg(reinterpret_cast<const float4*>(x.src + gi));
     if (x.add) {
@@ -583,12 +607,14 @@ ES_DEV float4 gvm_x4(const GvXSrc& x, int m, int k) {
         v.x += a.x; v.y += a.y; v.z += a.z; v.w += a.w;
     }
     if (x.kind == XS_NORM) {
-        const bf16* gp = (const bf16*)x.gain + k;
-        const float ri = __ldcg(x.rinv + m);
-        v.x *= ri * __bfloat162float(gp[0]);
-        v.y *= ri * __bfloat162float(gp[1]);
-        v.z *= ri * __bfloat162float(gp[2]);
-        v.w *= ri * __bfloat162float(gp[3]);
+        // four bf16 gains in one 8-byte load (k is a multiple of 4)
+        const uint2 gb = *reinterpret_cast<const uint2*>((const bf16*)x.gain + k);
+        // with partial sums, 1/rms is a per-row factor applied in the epilogue
+        const float ri = x.ss_tiles > 0 ? 1.0f : __ldcg(x.rinv + m);
+        v.x *= ri * __uint_as_float(gb.x << 16);
+        v.y *= ri * __uint_as_float(gb.x & 0xffff0000u);
+        v.z *= ri * __uint_as_float(gb.y << 16);
+        v.w *= ri * __uint_as_float(gb.y & 0xffff0000u);
     }
     return v;
 }
@@ -651,40 +677,44 @@ __host__ __device__ inline int gvm_windows(const GvLaunch& L, int S0, int S1, Gv
 }
 
 // Stage the windows with off >= 0 as hi/lo planes (whole CTA; synchronises).
-ES_DEV void gvm_stage(const GvLaunch& L, const GvmWin* win, int nwin, int nitems, unsigned char* xsm) {
+ES_DEV void gvm_stage(const GvLaunch& L, const GvmWin* win, int nwin, int nitems, unsigned char* xsm,
+                      const float* srinv) {
     const int M = L.M;
-    constexpr int SB = 8;
+    constexpr int SB = 16;  // items per thread with their loads in flight together
+    // item t -> (window, activation row m, column offset kr in the window)
+    auto locate = [&](int t, int& i, int& m, int& kr) {
+        i = 0;
+        while (win[i].off < 0 || t >= win[i].item0 + M * ((win[i].khi - win[i].klo) * (GVM_COLS / 4))) ++i;
+        const int C4 = (win[i].khi - win[i].klo) * (GVM_COLS / 4), r = t - win[i].item0;
+        m = r / C4;
+        kr = (r - m * C4) * 4;
+    };
     for (int t0 = threadIdx.x; t0 < nitems; t0 += SB * GV_THREADS) {
         float4 v[SB];
-        uint2* dh[SB];
-        int lo_off[SB];
 #pragma unroll
         for (int u = 0; u < SB; ++u) {
             const int t = t0 + u * GV_THREADS;
-            dh[u] = nullptr;
-            lo_off[u] = 0;
             v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (t < nitems) {
-                int i = 0;
-                while (win[i].off < 0 || t >= win[i].item0 + M * ((win[i].khi - win[i].klo) * (GVM_COLS / 4))) ++i;
-                const GvmWin& wd = win[i];
-                const GvXSrc& x = L.xs[wd.src];
-                const int C4 = (wd.khi - wd.klo) * (GVM_COLS / 4), r = t - wd.item0, m = r / C4;
-                const int kr = (r - m * C4) * 4, k = wd.klo * GVM_COLS + kr;
-                if (k < x.K) v[u] = gvm_x4(x, m, k);
-                bf16* plane = reinterpret_cast<bf16*>(xsm + (size_t)wd.off * 4);
-                dh[u] = reinterpret_cast<uint2*>(plane + (size_t)m * wd.pw + kr);
-                lo_off[u] = M * wd.pw;
+                int i, m, kr;
+                locate(t, i, m, kr);
+                const GvXSrc& x = L.xs[win[i].src];
+                const int k = win[i].klo * GVM_COLS + kr;
+                if (k < x.K) v[u] = gvm_x4(x, m, k, srinv);
             }
         }
 #pragma unroll
         for (int u = 0; u < SB; ++u) {
-            if (!dh[u]) continue;
+            const int t = t0 + u * GV_THREADS;
+            if (t >= nitems) break;
+            int i, m, kr;
+            locate(t, i, m, kr);
+            bf16* hi = reinterpret_cast<bf16*>(xsm + (size_t)win[i].off * 4) + (size_t)m * win[i].pw + kr;
             uint2 h, l;
             split2(v[u].x, v[u].y, h.x, l.x);
             split2(v[u].z, v[u].w, h.y, l.y);
-            *dh[u] = h;
-            *reinterpret_cast<uint2*>(reinterpret_cast<bf16*>(dh[u]) + lo_off[u]) = l;
+            *reinterpret_cast<uint2*>(hi) = h;
+            *reinterpret_cast<uint2*>(hi + (size_t)M * win[i].pw) = l;
         }
     }
     __syncthreads();
@@ -831,13 +861,14 @@ ES_DEV uint4 lds16(uint32_t a) {
 
 // B fragments (hi, lo) of group j of chunk C.kc read as float32 from
 // global memory: the fallback for sources without a staged window.
-ES_DEV void gvm_x_global(const GvLaunch& L, const GvmWarp& ws, const GvmCons& C, int j, uint4& bh, uint4& bl) {
+ES_DEV void gvm_x_global(const GvLaunch& L, const GvmWarp& ws, const GvmCons& C, int j, uint4& bh, uint4& bl,
+                         const float* srinv) {
     const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
     const GvXSrc& x = L.xs[ws.src];
     const int k = C.kc * GVM_COLS + 32 * j + 8 * c;
     bh = bl = make_uint4(0u, 0u, 0u, 0u);
     if (g < L.M && k < x.K) {
-        const float4 f0 = gvm_x4(x, g, k), f1 = gvm_x4(x, g, k + 4);
+        const float4 f0 = gvm_x4(x, g, k, srinv), f1 = gvm_x4(x, g, k + 4, srinv);
         split2(f0.x, f0.y, bh.x, bl.x);
         split2(f0.z, f0.w, bh.y, bl.y);
         split2(f1.x, f1.y, bh.z, bl.z);
@@ -853,7 +884,8 @@ ES_DEV void gvm_mma_group(float (&acc)[4], const uint4& a, const uint4& b, const
 }
 
 // acc += W(chunk C.kc of this warp's rows) . x, and step.
-ES_DEV void gvm_cons_step(const GvLaunch& L, const GvmWarp& ws, GvmCons& C, const GvmStage& st, float (&acc)[4]) {
+ES_DEV void gvm_cons_step(const GvLaunch& L, const GvmWarp& ws, GvmCons& C, const GvmStage& st, float (&acc)[4],
+                          const float* srinv) {
     if (!C.glob) {
         const uint32_t a0 = C.sa + (uint32_t)(C.kc * GVM_COLS - C.kbase) * 2u;
         uint4 bh[4], bl[4];
@@ -868,30 +900,106 @@ ES_DEV void gvm_cons_step(const GvLaunch& L, const GvmWarp& ws, GvmCons& C, cons
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             uint4 bh, bl;
-            gvm_x_global(L, ws, C, j, bh, bl);
+            gvm_x_global(L, ws, C, j, bh, bl, srinv);
             gvm_mma_group(acc, st.a[j], st.b[j], bh, bl);
         }
     }
     ++C.kc;
 }
 
+// The op reads normalised sources with partial sums: its sums get 1/rms of
+// the activation row in the epilogue (all of an op's segments read the same
+// kind of source).
+ES_DEV bool gvm_op_scaled(const GvLaunch& L, const GvOp& o) {
+    const GvXSrc& x = L.xs[L.segs[o.seg0].xs];
+    return x.kind == XS_NORM && x.ss_tiles > 0;
+}
+
 // Epilogue of one 16-row tile from the D fragments: lane (g, c) holds rows
-// (n0+g, n0+g+8) x activation rows (2c, 2c+1).
-ES_DEV void gvm_epilogue(const GvLaunch& L, const GvOp& o, int n0, const float (&v0)[4], const float (&v1)[4]) {
+// (n0+g, n0+g+8) x activation rows (2c, 2c+1).  With `ss`, also the sums of
+// squares of the post-norm's input (h + add) over these 16 columns, per
+// activation row, for the next launch's normalisation (deterministic: a
+// fixed shuffle order).
+ES_DEV void gvm_epilogue(const GvLaunch& L, const GvOp& o, int n0, const float (&v0)[4], const float (&v1)[4],
+                         bool ss, const float* srinv) {
     const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+    const bool scaled = gvm_op_scaled(L, o);
+    float sq[2] = {0.f, 0.f};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
         const int m = 2 * c + (e & 1), n = n0 + g + (e >> 1) * 8;
         if (m >= L.M || n >= o.N) continue;
         float* y = o.y + (size_t)m * o.ldy + n;
+        const float f = scaled ? srinv[m] : 1.0f;
+        const float r0 = v0[e] * f, r1 = v1[e] * f;
+        float out;
         switch (o.epi) {
-            case GEPI_STORE: *y = v0[e]; break;
-            case GEPI_ACC: *y = __ldcg(y) + v0[e]; break;
-            case GEPI_ACC_ADD: *y = __ldcg(y) + v0[e] + __ldcg(o.add + (size_t)m * o.ldy + n); break;
-            default: *y = silu_f(v0[e]) * v1[e]; break;
+            case GEPI_STORE: out = r0; break;
+            case GEPI_ACC: out = __ldcg(y) + r0; break;
+            case GEPI_ACC_ADD: out = __ldcg(y) + r0 + __ldcg(o.add + (size_t)m * o.ldy + n); break;
+            default: out = silu_f(r0) * r1; break;
+        }
+        *y = out;
+        if (ss) {
+            const GvPost& p = L.post;
+            const size_t i = (size_t)m * p.K + n;
+            float t = o.y == p.h ? out : __ldcg(p.h + i);
+            if (p.add) t += o.y == p.add ? out : __ldcg(p.add + i);
+            sq[e & 1] += t * t;
+        }
+    }
+    if (ss) {
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], off);
+            sq[1] += __shfl_xor_sync(0xffffffffu, sq[1], off);
+        }
+        if (g == 0) {
+            float* dst = L.post.ssp + (size_t)(n0 / GVM_ROWS) * L.M;
+            if (2 * c < L.M) dst[2 * c] = sq[0];
+            if (2 * c + 1 < L.M) dst[2 * c + 1] = sq[1];
         }
     }
 }
+
+// 1/rms of this launch's normalised rows from the producer's sums of squares
+// (first XS_NORM source with partials; all of a launch's normalised sources
+// share h, add and rows).  Warp m handles row m: gvm_rinv_issue requests up
+// to 8 partials per lane before the staging, gvm_rinv_finish adds them (and
+// any further ones) lane-strided, then in a fixed shuffle order, so every CTA
+// gets the same value.
+struct GvmRinv { float r[8]; int xi; };
+
+ES_DEV void gvm_rinv_issue(const GvLaunch& L, GvmRinv& R) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    R.xi = -1;
+    for (int i = 0; i < L.nxs; ++i)
+        if (L.xs[i].kind == XS_NORM && L.xs[i].ss_tiles > 0) { R.xi = i; break; }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) R.r[u] = 0.f;
+    if (R.xi < 0 || warp >= L.M) return;
+    const GvXSrc& x = L.xs[R.xi];
+    const int pr = warp * x.row_stride + x.row_off;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int i = lane + 32 * u;
+        if (i < x.ss_tiles) R.r[u] = __ldcg(x.rinv + (size_t)i * x.ss_ld + pr);
+    }
+}
+
+ES_DEV void gvm_rinv_finish(const GvLaunch& L, const GvmRinv& R, float* srinv) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (R.xi < 0 || warp >= L.M) return;
+    const GvXSrc& x = L.xs[R.xi];
+    const int pr = warp * x.row_stride + x.row_off;
+    float t = 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) t += R.r[u];
+    for (int i = lane + 256; i < x.ss_tiles; i += 32) t += __ldcg(x.rinv + (size_t)i * x.ss_ld + pr);
+    t = warp_sum(t);
+    if (lane == 0) srinv[warp] = 1.0f / sqrtf(t / (float)x.K + x.eps);
+}
+
 
 __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM)
 gvm_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __restrict__ counters,
@@ -900,6 +1008,7 @@ gvm_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __
     __shared__ __align__(16) GvLaunch L;
     __shared__ GvmWin win[GVM_NWIN];
     __shared__ GvmWarp wstate[GV_WARPS];
+    __shared__ float srinv[GV_MAXM];
     __shared__ int s_nwin, s_items, s_last, s_done;
     gv_load_desc(L, Lg);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -925,7 +1034,13 @@ gvm_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __
     grid_dep_wait();
     grid_dep_launch();
     const int nwin = s_nwin;
-    gvm_stage(L, win, nwin, s_items, gvm_xsm);
+    {
+        GvmRinv R;
+        gvm_rinv_issue(L, R);
+        gvm_stage(L, win, nwin, s_items, gvm_xsm, srinv);  // ends with a barrier
+        gvm_rinv_finish(L, R, srinv);
+        __syncthreads();
+    }
 
     GvmCons C;
     gvm_cons_begin(L, ws, C, win, nwin, gvm_xsm, S1);
@@ -940,8 +1055,8 @@ gvm_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __
                 gvm_issue_step(L, ws, I, ring[(i + GVM_D - 1) % GVM_D], S1);
                 ++s_issue;
             }
-            if (C.set == 0) gvm_cons_step(L, ws, C, ring[i], acc0);
-            else gvm_cons_step(L, ws, C, ring[i], acc1);
+            if (C.set == 0) gvm_cons_step(L, ws, C, ring[i], acc0, srinv);
+            else gvm_cons_step(L, ws, C, ring[i], acc1, srinv);
             if (C.kc < C.kc_end) continue;
             if (C.tile_end || si + 1 == S1) {
                 // ---- finish the block (or this CTA's part of it); CTA-uniform
@@ -954,14 +1069,13 @@ gvm_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __
                     float* part = scratch + ((size_t)((cta * 2 + sid) * GV_WARPS + warp) * 2) * 128 + lane * 4;
                     *reinterpret_cast<float4*>(part) = make_float4(acc0[0], acc0[1], acc0[2], acc0[3]);
                     if (two) *reinterpret_cast<float4*>(part + 128) = make_float4(acc1[0], acc1[1], acc1[2], acc1[3]);
-                    __threadfence();
                     __syncthreads();
                     const int c_first = blk_first / q, c_last = blk_last / q;
                     const int gblk = o.tile0 + ws.tile;
-                    if (tid == 0) s_last = atomicAdd(counters + gblk, 1) == c_last - c_first;
+                    const int old = cta_arrive(counters + gblk);
+                    if (tid == 0) s_last = old == c_last - c_first;
                     __syncthreads();
                     if (s_last) {
-                        __threadfence();
 #pragma unroll
                         for (int e = 0; e < 4; ++e) acc0[e] = acc1[e] = 0.f;
                         // partials of CTAs c_first..c_last, summed in CTA order;
@@ -999,7 +1113,9 @@ gvm_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __
                     // every thread has read s_last before a later block changes it
                     __syncthreads();
                 }
-                if (do_epi) gvm_epilogue(L, o, ws.tile * GVM_BLOCK + warp * GVM_ROWS, acc0, acc1);
+                if (do_epi)
+                    gvm_epilogue(L, o, ws.tile * GVM_BLOCK + warp * GVM_ROWS, acc0, acc1,
+                                 L.post.ssp != nullptr && ws.op == L.post.op, srinv);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc0[e] = acc1[e] = 0.f;
                 blk_first = blk_last + 1;
@@ -1007,13 +1123,12 @@ gvm_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __
             if (si + 1 < S1) gvm_cons_begin(L, ws, C, win, nwin, gvm_xsm, S1);
         }
     }
-    if (L.post.rows > 0) {
-        __threadfence();
+    if (L.post.rows > 0 && !L.post.ssp) {
         __syncthreads();
-        if (tid == 0) s_done = atomicAdd(done, 1) == (int)gridDim.x - 1;
+        const int old = cta_arrive(done);
+        if (tid == 0) s_done = old == (int)gridDim.x - 1;
         __syncthreads();
         if (s_done) {
-            __threadfence();
             post_rinv(L.post);
             if (tid == 0) *done = 0;
         }

@@ -85,7 +85,10 @@ ES_DEV void embed_item(const EmbedArgs& a, int m) {
     // 1/rms of the embedded rows for the first weight pass
     if (a.post.rows > 0) {
         ss = block_sum(ss, red);
-        if (threadIdx.x == 0) a.post.rinv[m] = 1.0f / sqrtf(ss / (float)d + a.post.eps);
+        if (threadIdx.x == 0) {
+            if (a.post.ssp) a.post.ssp[m] = ss;  // one partial per row
+            else a.post.rinv[m] = 1.0f / sqrtf(ss / (float)d + a.post.eps);
+        }
     }
 }
 
