@@ -72,7 +72,6 @@ ES_DEV void attn_item(const AttnArgs& a, int m, int jy, int sp) {
     const int pos = __ldcg(a.row_pos + m);
     const int p0 = sp * PAGE;
     if (pos < 0 || p0 > pos) return;
-    __syncthreads();  // the previous item of this CTA is done with shared memory
     const int n = min(PAGE, pos + 1 - p0);
     const int rb = __ldcg(a.row_base + m), bpos = __ldcg(a.row_pos + rb), seq = __ldcg(a.row_seq + m);
     const int tid = threadIdx.x, layer = a.layer[j];
@@ -93,18 +92,26 @@ ES_DEV void attn_item(const AttnArgs& a, int m, int jy, int sp) {
     const T* Vp = kv_ptr<T>(a.g, seq, p0, layer, 1, hk);
     const float* q = a.q[j] + (size_t)m * qd + (size_t)hk * G * hd;
     const float* csq = a.rope + (size_t)pos * hd;
-    for (int base = 0; base < (cached ? nv : 0) || base == 0; base += VPT * ATT_THREADS) {
-        uint4 kv4[VPT], vv4[VPT];
-        if (cached) {
+    // A cached page was written by earlier launches, and the row
+    // descriptors by the embedding kernel, which finished before the weight
+    // pass that launched this kernel: the first pass of page loads is
+    // issued before waiting for that weight pass (the queries are not).
+    uint4 kv4[VPT], vv4[VPT];
+    auto load_pass = [&](int base) {
 #pragma unroll
-            for (int u = 0; u < VPT; ++u) {
-                const int t = base + u * ATT_THREADS + tid;
-                if (t < nv) {
-                    kv4[u] = __ldcg(reinterpret_cast<const uint4*>(Kp + (size_t)t * EPV));
-                    vv4[u] = __ldcg(reinterpret_cast<const uint4*>(Vp + (size_t)t * EPV));
-                }
+        for (int u = 0; u < VPT; ++u) {
+            const int t = base + u * ATT_THREADS + tid;
+            if (t < nv) {
+                kv4[u] = __ldcg(reinterpret_cast<const uint4*>(Kp + (size_t)t * EPV));
+                vv4[u] = __ldcg(reinterpret_cast<const uint4*>(Vp + (size_t)t * EPV));
             }
         }
+    };
+    if (cached) load_pass(0);
+    grid_dep_wait();
+    grid_dep_launch();
+    for (int base = 0; base < (cached ? nv : 0) || base == 0; base += VPT * ATT_THREADS) {
+        if (cached && base > 0) load_pass(base);
         if (base == 0) {
             for (int t = tid; t < G * half; t += ATT_THREADS) {
                 const int h = t / half, i = t % half;
@@ -215,14 +222,14 @@ ES_DEV void attn_item(const AttnArgs& a, int m, int jy, int sp) {
         else part_row[((size_t)h * a.nsplit + sp) * (hd + 2) + e] = acc;
     }
     if (nact == 1) return;
-    // last arriving split of (m, j, kv head) merges the partials
-    __threadfence();
+    // last arriving split of (m, j, kv head) merges the partials (one
+    // acquire-release arrival per CTA after the barrier)
     __syncthreads();
     int* ctr = a.counters + ((size_t)m * a.nl + j) * Hkv + hk;
-    if (tid == 0) s_last = atomicAdd(ctr, 1) == nact - 1;
+    const int old = cta_arrive(ctr);
+    if (tid == 0) s_last = old == nact - 1;
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
     // merge weights w[h][p] = exp(m_p - max) / sum_p' exp(m_p' - max) l_p'
     // (reusing the score buffer: nact <= nsplit splits per head)
     float* wsm = sc;
@@ -258,10 +265,10 @@ ES_DEV void attn_item(const AttnArgs& a, int m, int jy, int sp) {
     if (tid == 0) *ctr = 0;
 }
 
+// One CTA per work item; attn_item waits for the preceding kernel itself
+// (after requesting the cached K/V page).
 template <typename T>
 __global__ void __launch_bounds__(ATT_THREADS) attn_kernel(AttnArgs a) {
-    grid_dep_wait();
-    grid_dep_launch();
     attn_item<T>(a, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 

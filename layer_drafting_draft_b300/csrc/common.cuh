@@ -40,6 +40,19 @@ ES_DEV void unpack16(const uint4& v, float* out, bf16) {
     }
 }
 
+// Arrival of a whole CTA at a counter shared by several CTAs: after the
+// barrier, one release-acquire atomic by thread 0 publishes every thread's
+// earlier writes (the barrier orders them before the release) and, for the
+// last arriver, makes the other CTAs' writes visible to it (its threads read
+// them after the barrier that follows).  Returns the counter's old value to
+// thread 0 (undefined elsewhere).
+ES_DEV int cta_arrive(int* ctr) {
+    int old = 0;
+    if (threadIdx.x == 0)
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(ctr) : "memory");
+    return old;
+}
+
 // ---------------------------------------------------------------- reductions
 ES_DEV float warp_sum(float v) {
 #pragma unroll

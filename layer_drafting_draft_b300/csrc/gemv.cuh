@@ -170,18 +170,6 @@ ES_DEV float warp_reduce_scatter(const float (&v)[NV], int lane) {
     return a[0];
 }
 
-// Arrival of a whole CTA at a counter shared by several CTAs: after the
-// barrier, one release-acquire atomic by thread 0 publishes every thread's
-// earlier writes (the barrier orders them before the release) and, for the
-// last arriver, makes the other CTAs' writes visible to it (its threads read
-// them after the barrier that follows).  Returns the counter's old value to
-// thread 0 (undefined elsewhere).
-ES_DEV int cta_arrive(int* ctr) {
-    int old = 0;
-    if (threadIdx.x == 0)
-        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(ctr) : "memory");
-    return old;
-}
 
 // ------------------------------------------------------------ post-norm
 // Executed by one whole CTA (GV_THREADS threads) once the rows it reads are
