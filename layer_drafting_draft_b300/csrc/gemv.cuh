@@ -665,10 +665,10 @@ __host__ __device__ inline int gvm_windows(const GvLaunch& L, int S0, int S1, Gv
 }
 
 // Stage the windows with off >= 0 as hi/lo planes (whole CTA; synchronises).
+template <int SB>  // items per thread with their loads in flight together
 ES_DEV void gvm_stage(const GvLaunch& L, const GvmWin* win, int nwin, int nitems, unsigned char* xsm,
                       const float* srinv) {
     const int M = L.M;
-    constexpr int SB = 16;  // items per thread with their loads in flight together
     // item t -> (window, activation row m, column offset kr in the window)
     auto locate = [&](int t, int& i, int& m, int& kr) {
         i = 0;
@@ -1021,11 +1021,15 @@ gvm_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __
     __syncthreads();
     grid_dep_wait();
     grid_dep_launch();
+    // the ring's other stage goes out before the staging round trips
+#pragma unroll
+    for (int i = GVM_D - 1; i < GVM_D; ++i)
+        if (s_issue < S1) { gvm_issue_step(L, ws, I, ring[i], S1); ++s_issue; }
     const int nwin = s_nwin;
     {
         GvmRinv R;
         gvm_rinv_issue(L, R);
-        gvm_stage(L, win, nwin, s_items, gvm_xsm, srinv);  // ends with a barrier
+        gvm_stage<8>(L, win, nwin, s_items, gvm_xsm, srinv);  // ends with a barrier
         gvm_rinv_finish(L, R, srinv);
         __syncthreads();
     }
@@ -1039,12 +1043,13 @@ gvm_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __
         for (int i = 0; i < GVM_D; ++i) {
             const int si = s + i;
             if (si >= S1) break;
-            if (s_issue < S1) {  // keep GVM_D - 1 stages ahead in flight
-                gvm_issue_step(L, ws, I, ring[(i + GVM_D - 1) % GVM_D], S1);
-                ++s_issue;
-            }
             if (C.set == 0) gvm_cons_step(L, ws, C, ring[i], acc0, srinv);
             else gvm_cons_step(L, ws, C, ring[i], acc1, srinv);
+            // refill the slot just multiplied: GVM_D stages stay in flight
+            if (s_issue < S1) {
+                gvm_issue_step(L, ws, I, ring[i], S1);
+                ++s_issue;
+            }
             if (C.kc < C.kc_end) continue;
             if (C.tile_end || si + 1 == S1) {
                 // ---- finish the block (or this CTA's part of it); CTA-uniform
