@@ -1,5 +1,6 @@
 // libeasyspec: host runtime and C ABI for EasySpec layer-parallel
 // speculative decoding on one B300.  See include/easyspec.h for the contract.
+#include <cublas_v2.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -53,6 +54,7 @@ struct Rec {
     double bytes = 0;          // algorithmic bytes (weights + activations), 0 if not modelled
     const GvLaunch* gv = nullptr;           // device copy (after upload)
     std::shared_ptr<GvLaunch> host;         // host copy while the plan is built
+    std::shared_ptr<GvLaunch> gemm_ops;     // many-row passes: the ops, kept on the host
     bool bf16 = false;                      // weights are bf16
     int grid = 0, smem = 0, M = 0, ntiles64 = 0;
     NormArgs norm{};
@@ -93,6 +95,13 @@ struct Graph { cudaGraphExec_t exec = nullptr; int64_t kernels = 0; };
 struct es_ctx {
     es_config cfg{};
     Model md, mb;
+    // many-row bf16 passes (prompt prefill, batches past 8 rows): cuBLAS
+    // tensor-core GEMMs on hi/lo activation planes
+    cublasHandle_t blas = nullptr;
+    void* blas_ws = nullptr;
+    size_t blas_ws_bytes = 0;
+    bf16 *tc_hi = nullptr, *tc_lo = nullptr;
+    float *tc_g = nullptr, *tc_u = nullptr;
     cudaStream_t st = nullptr;
     bool own_stream = false;
     int dev = 0, num_sms = 148;
@@ -449,6 +458,7 @@ void upload_plan(es_ctx* c, Plan& p) {
         CK(cudaMemcpy(c->arena + at, r.host.get(), bytes, cudaMemcpyHostToDevice));
         c->arena_used = at + bytes;
         r.gv = reinterpret_cast<const GvLaunch*>(c->arena + at);
+        if (r.kind == R_GEMM) r.gemm_ops = r.host;
         r.host.reset();
     }
 }
@@ -663,6 +673,70 @@ std::vector<std::vector<int>> default_sets(int L, int k) {
 }
 
 // ------------------------------------------------------------------ launches
+void blas_check(cublasStatus_t st, int line) {
+    if (st != CUBLAS_STATUS_SUCCESS) arg_fail(ES_ERR_CUDA, "cuBLAS status %d at line %d", (int)st, line);
+}
+
+// A many-row weight pass with bf16 weights: for each op and segment, the
+// segment's activations are split into bf16 hi/lo planes and
+// y (+)= W . hi + W . lo runs as two cuBLAS GEMMs (bf16 in, float32
+// accumulate and out, tensor cores); residual adds and SwiGLU follow as one
+// elementwise kernel.  Row-major y[M][N] = x[M][K] . W[N][K]^T is the
+// column-major product W^T(K x N, transposed) . x(K x M).
+void gemm_many_rows(es_ctx* c, const Rec& r) {
+    const GvLaunch& L = *r.gemm_ops;
+    const int M = L.M;
+    cudaEvent_t ev0 = nullptr, ev1 = nullptr;
+    if (c->profiling) {
+        if (c->prof_pool_used == c->prof_pool.size()) {
+            cudaEvent_t x, y;
+            CK(cudaEventCreate(&x));
+            CK(cudaEventCreate(&y));
+            c->prof_pool.emplace_back(x, y);
+        }
+        ev0 = c->prof_pool[c->prof_pool_used].first;
+        ev1 = c->prof_pool[c->prof_pool_used].second;
+        c->prof_pool_used++;
+        CK(cudaEventRecord(ev0, c->st));
+    }
+    blas_check(cublasSetStream(c->blas, c->st), __LINE__);
+    for (int oi = 0; oi < L.nops; ++oi) {
+        const GvOp& o = L.ops[oi];
+        const bool swi = o.epi == GEPI_SWIGLU;
+        float* tgt[2] = {swi ? c->tc_g : o.y, c->tc_u};
+        const int ldt[2] = {swi ? o.N : o.ldy, o.N};
+        bool first[2] = {o.epi == GEPI_STORE || swi, true};  // beta = 0 for the first product
+        for (int si = 0; si < o.nseg; ++si) {
+            const GvSeg& sg = L.segs[o.seg0 + si];
+            const GvXSrc& x = L.xs[sg.xs];
+            if (x.K != sg.K || sg.K % 4) arg_fail(ES_ERR_ARG, "internal: many-row segment width %d", sg.K);
+            const int items = M * (sg.K / 4);
+            launch(c, "split_hilo", 0.0, split_hilo_kernel, dim3(std::min(4 * c->num_sms, (items + 255) / 256)),
+                   dim3(256), (size_t)0, x.src, x.ld, x.row_stride, x.row_off, M, sg.K, c->tc_hi, c->tc_lo);
+            const int set = sg.set;
+            const float one = 1.0f, zero = 0.0f;
+            for (int plane = 0; plane < 2; ++plane) {
+                const float* beta = first[set] ? &zero : &one;
+                blas_check(cublasGemmEx(c->blas, CUBLAS_OP_T, CUBLAS_OP_N, o.N, M, sg.K, &one, sg.W, CUDA_R_16BF,
+                                        sg.K, plane ? c->tc_lo : c->tc_hi, CUDA_R_16BF, sg.K, beta, tgt[set],
+                                        CUDA_R_32F, ldt[set], CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT),
+                           __LINE__);
+                first[set] = false;
+            }
+        }
+        if (swi || o.epi == GEPI_ACC_ADD) {
+            const int n = M * o.N;
+            launch(c, "epi_rows", 0.0, epi_rows_kernel, dim3(std::min(4 * c->num_sms, (n + 255) / 256)), dim3(256),
+                   (size_t)0, o.y, o.ldy, swi ? nullptr : o.add, swi ? c->tc_g : nullptr,
+                   swi ? c->tc_u : nullptr, M, o.N);
+        }
+    }
+    if (c->profiling) {
+        CK(cudaEventRecord(ev1, c->st));
+        c->prof_pending.push_back(ProfRec{r.name, r.bytes, ev0, ev1});
+    }
+}
+
 template <typename T>
 void run_rec(es_ctx* c, const Rec& r) {
     switch (r.kind) {
@@ -685,8 +759,12 @@ void run_rec(es_ctx* c, const Rec& r) {
             }
             break;
         case R_GEMM:
-            launch(c, "gemm_simt", r.bytes, gemm_kernel<T>, dim3(r.ntiles64, (r.M + GB - 1) / GB), dim3(256),
-                   (size_t)0, r.gv);
+            if constexpr (std::is_same<T, bf16>::value) {
+                gemm_many_rows(c, r);
+            } else {
+                launch(c, "gemm_simt", r.bytes, gemm_kernel<T>, dim3(r.ntiles64, (r.M + GB - 1) / GB),
+                       dim3(256), (size_t)0, r.gv);
+            }
             break;
         case R_NORM:
             launch(c, r.name, 0.0, norm_kernel<T>, dim3(r.M), dim3(256), (size_t)0, r.norm);
@@ -1173,6 +1251,25 @@ es_status easyspec_init(const es_config* cfg, const es_weights* draft, const es_
         c->arena_cap = (size_t)64 << 20;
         c->arena = c->dalloc<char>(c->arena_cap);
         c->gv_scratch = c->dalloc<float>(std::max(GV_SCRATCH_FLOATS, GVM_SCRATCH_FLOATS));
+        if (c->md.dtype == ES_DTYPE_BF16 || c->mb.dtype == ES_DTYPE_BF16) {
+            // many-row bf16 passes: cuBLAS with a fixed workspace (so they can
+            // be captured in CUDA graphs) and the hi/lo / SwiGLU buffers
+            size_t rows = 0, kmax = 0, fmax = 0;
+            for (const Model* mm : {&c->md, &c->mb}) {
+                rows = std::max(rows, (size_t)mm->Mw);
+                kmax = std::max({kmax, (size_t)mm->d, (size_t)mm->qd, (size_t)mm->F});
+                fmax = std::max(fmax, (size_t)mm->F);
+            }
+            if (cublasCreate(&c->blas) != CUBLAS_STATUS_SUCCESS) arg_fail(ES_ERR_CUDA, "cublasCreate failed");
+            c->blas_ws_bytes = (size_t)32 << 20;
+            c->blas_ws = c->dalloc<char>(c->blas_ws_bytes);
+            blas_check(cublasSetWorkspace(c->blas, c->blas_ws, c->blas_ws_bytes), __LINE__);
+            blas_check(cublasSetStream(c->blas, c->st), __LINE__);
+            c->tc_hi = c->dalloc<bf16>(rows * kmax);
+            c->tc_lo = c->dalloc<bf16>(rows * kmax);
+            c->tc_g = c->dalloc<float>(rows * fmax);
+            c->tc_u = c->dalloc<float>(rows * fmax);
+        }
         c->gv_counters = c->dalloc<int>(GV_COUNTERS);
         c->gv_done = c->dalloc<int>(1);
         c->att_counters = c->dalloc<int>(ATT_COUNTERS);
@@ -1493,6 +1590,7 @@ void easyspec_destroy(es_ctx* c) {
     if (c->h_prm) cudaFreeHost(c->h_prm);
     if (c->h_small) cudaFreeHost(c->h_small);
     if (c->cfg.group_starts) delete[] c->cfg.group_starts;
+    if (c->blas) cublasDestroy(c->blas);
     if (c->own_stream) cudaStreamDestroy(c->st);
     delete c;
 }

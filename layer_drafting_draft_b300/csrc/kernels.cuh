@@ -98,6 +98,46 @@ __global__ void prep_embed_kernel(EmbedArgs a) {
     if (blockIdx.x < a.M) embed_item<T>(a, blockIdx.x);
 }
 
+// ------------------------------------------------------- many-row helpers
+// Row m of a source (row m*rs + ro of src, leading dimension ld) split into
+// bf16 hi/lo planes [M][K]: hi = bf16(x), lo = bf16(x - hi), so a bf16
+// tensor-core GEMM of each plane, summed, keeps ~16 significant bits of x.
+__global__ void split_hilo_kernel(const float* __restrict__ src, int ld, int rs, int ro, int M, int K,
+                                  bf16* __restrict__ hi, bf16* __restrict__ lo) {
+    grid_dep_wait();
+    grid_dep_launch();
+    const int K4 = K >> 2;
+    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < M * K4; t += gridDim.x * blockDim.x) {
+        const int m = t / K4, k = (t - m * K4) * 4;
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(m * rs + ro) * ld + k));
+        const __nv_bfloat162 h0 = __floats2bfloat162_rn(v.x, v.y), h1 = __floats2bfloat162_rn(v.z, v.w);
+        const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+        const __nv_bfloat162 l0 = __floats2bfloat162_rn(v.x - f0.x, v.y - f0.y);
+        const __nv_bfloat162 l1 = __floats2bfloat162_rn(v.z - f1.x, v.w - f1.y);
+        __nv_bfloat162* ph = reinterpret_cast<__nv_bfloat162*>(hi + (size_t)m * K + k);
+        __nv_bfloat162* pl = reinterpret_cast<__nv_bfloat162*>(lo + (size_t)m * K + k);
+        ph[0] = h0; ph[1] = h1; pl[0] = l0; pl[1] = l1;
+    }
+}
+
+// Epilogues of a many-row weight pass after its GEMMs: y += add
+// (residual + delta) or y = silu(g) * u (SwiGLU); y [M][ldy], g/u [M][N].
+__global__ void epi_rows_kernel(float* __restrict__ y, int ldy, const float* __restrict__ add,
+                                const float* __restrict__ g, const float* __restrict__ u, int M, int N) {
+    grid_dep_wait();
+    grid_dep_launch();
+    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < M * N; t += gridDim.x * blockDim.x) {
+        const int m = t / N, n = t - m * N;
+        float* yp = y + (size_t)m * ldy + n;
+        if (g) {
+            const float a = g[t];
+            *yp = a / (1.0f + expf(-a)) * u[t];
+        } else {
+            *yp += add[(size_t)m * ldy + n];
+        }
+    }
+}
+
 // -------------------------------------------------------------------- RMSNorm
 // out_j[r] = RMSNorm(h[src], g_j) for every job j, with src = r*stride + off.
 // If `add` is set, h[src] += add[src] first (written back).
