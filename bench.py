@@ -58,6 +58,8 @@ def parse():
     ap.add_argument("--mode", default="full", choices=["full", "attn"])
     ap.add_argument("--temperature", type=float, default=1.0)
     ap.add_argument("--gamma", type=int, default=None)
+    ap.add_argument("--batch", type=int, default=1,
+                    help="sequences decoded together (the batched long-context workload: 1, 4 or 16)")
     ap.add_argument("--sigma", type=float, default=None,
                     help="self-draft workloads: draft = base + N(0, (sigma*0.02)^2)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -83,14 +85,17 @@ def shape_str(s: dict) -> str:
             f"ffn{s['ffn']} V{s['vocab']}")
 
 
-def phase_bytes(wl: dict, gamma: int, ctx: int) -> dict:
+def phase_bytes(wl: dict, gamma: int, ctx: int, B: int = 1) -> dict:
+    """Bytes one phase must move for B sequences: the weights once, the KV
+    and embedding rows per sequence."""
     esz = 2 if wl["dtype"] == "bf16" else 4
     wd, wb = weight_bytes(wl["draft"], esz), weight_bytes(wl["base"], esz)
-    draft_fwd = wd["layers"] + wd["head"] + wd["embed_row"]
-    draft = gamma * draft_fwd + kv_bytes(wl["draft"], esz, ctx, 2 * gamma)
-    # the gamma - 1 fuzzy forwards alone (one row each)
-    fuzzy = (gamma - 1) * draft_fwd + kv_bytes(wl["draft"], esz, ctx, gamma - 1)
-    verify = wb["layers"] + wb["head"] + (gamma + 1) * wb["embed_row"] + kv_bytes(wl["base"], esz, ctx, gamma + 1)
+    draft_fwd = wd["layers"] + wd["head"] + B * wd["embed_row"]
+    draft = gamma * draft_fwd + B * kv_bytes(wl["draft"], esz, ctx, 2 * gamma)
+    # the gamma - 1 fuzzy forwards alone (one row per sequence each)
+    fuzzy = (gamma - 1) * draft_fwd + B * kv_bytes(wl["draft"], esz, ctx, gamma - 1)
+    verify = (wb["layers"] + wb["head"] + B * (gamma + 1) * wb["embed_row"]
+              + B * kv_bytes(wl["base"], esz, ctx, gamma + 1))
     return {"draft_fwd": draft_fwd, "draft": draft, "fuzzy": fuzzy, "verify": verify}
 
 
@@ -224,11 +229,14 @@ def run_ours(args, rank: int, world: int):
     gamma = args.gamma or wl["gamma"]
     P, max_new, T, k = wl["prompt"], wl["max_new"], args.temperature, args.k
     draft_w, base_w, prompts = synth.make_pair(args.workload, device="cuda", sigma=args.sigma)
-    prompts = prompts[:1].numpy() if wl["batch"] >= 1 else prompts.numpy()
+    B = args.batch
+    if B > prompts.shape[0]:
+        raise SystemExit(f"--batch {B}: the workload has {prompts.shape[0]} prompts")
+    prompts = prompts[:B].numpy()
     stream = torch.cuda.Stream()
     mode = ES_FULL_LAYER if args.mode == "full" else ES_ATTN_ONLY
     max_seq = ((P + max_new + 2 * gamma + 2) + 63) // 64 * 64
-    g = EasySpec(draft_w, wl["draft"], base_w, wl["base"], wl["dtype"], 1, max_seq, gamma, mode,
+    g = EasySpec(draft_w, wl["draft"], base_w, wl["base"], wl["dtype"], B, max_seq, gamma, mode,
                  None, stream)
     seed0 = 1000 * rank
 
@@ -259,13 +267,13 @@ def run_ours(args, rank: int, world: int):
     clk = clocks.stop()
     barrier(world)
     total_ms = max_over_ranks(sum(dec_ms), world)
-    value = world * args.steps * max_new / (total_ms / 1e3)
+    value = world * args.steps * B * max_new / (total_ms / 1e3)
     emitted = sum(s["emitted"] for s in stats)
     phases = sum(s["phases"] for s in stats)
     accepted = sum(s["accepted"] for s in stats)
     drafted = sum(s["drafted"] for s in stats)
     launches = sum(s["kernel_launches"] for s in stats)
-    tok_per_phase = emitted / max(phases, 1)
+    tok_per_phase = emitted / max(phases * B, 1)  # per sequence
 
     # ---- per-phase breakdown: one more generation with the library's part
     # timing (CUDA events around each phase part's graph launch, calibration
@@ -281,12 +289,12 @@ def run_ours(args, rank: int, world: int):
     verify_ms = parts["phase.verify"][0] / nph
     draft_ms = calib_ms + fuzzy_ms
     peak, peak_src = peaks()
-    pb = phase_bytes(wl, gamma, P + max_new // 2)
+    pb = phase_bytes(wl, gamma, P + max_new // 2, B)
     draft_gbs = pb["draft"] / (draft_ms * 1e-3) / 1e9
     fuzzy_gbs = pb["fuzzy"] / (fuzzy_ms * 1e-3) / 1e9
     verify_gbs = pb["verify"] / (verify_ms * 1e-3) / 1e9
     phase_roof_s = (pb["draft"] + pb["verify"]) / (peak * 1e9)
-    roof_tok_s = tok_per_phase / phase_roof_s
+    roof_tok_s = B * tok_per_phase / phase_roof_s
 
     # ---- e2e through generate() with host buffers
     e2e_ms = []
@@ -296,7 +304,7 @@ def run_ours(args, rank: int, world: int):
         t0 = time.perf_counter()
         out_host, _ = g.generate(prompts, max_new, gamma, k, T, seed0 + 500 + s)
         e2e_ms.append((time.perf_counter() - t0) * 1e3)
-    e2e_value = world * max_new / (max_over_ranks(statistics.mean(e2e_ms), world) / 1e3)
+    e2e_value = world * B * max_new / (max_over_ranks(statistics.mean(e2e_ms), world) / 1e3)
 
     # ---- dominant kernel: per-launch event pass over one generation
     g.easyspec_prefill(prompts)
@@ -316,18 +324,18 @@ def run_ours(args, rank: int, world: int):
         "ms_per_step": round(total_ms / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl["dtype"], "data": "synthetic",
         "config": {"workload": args.workload, "draft": shape_str(wl["draft"]), "base": shape_str(wl["base"]),
-                   "batch": 1, "prompt": P, "max_new": max_new, "gamma": gamma, "k": k, "mode": args.mode,
+                   "batch": B, "prompt": P, "max_new": max_new, "gamma": gamma, "k": k, "mode": args.mode,
                    "temperature": T, "sigma": args.sigma, "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2 (weights {(pb['draft'] + pb['verify']) / 1e9:.1f} GB "
                          f"streamed per phase)"},
         "e2e": {"value": round(e2e_value, 2), "unit": "tok/s",
                 "h2d_bytes_per_step": int(prompts.size * 4 + 16 + 8),
-                "d2h_bytes_per_step": int(max_new * 4)},
-        "draft": {"tok_s": round(gamma / (draft_ms * 1e-3), 1), "ms_per_phase": round(draft_ms, 4),
+                "d2h_bytes_per_step": int(B * max_new * 4)},
+        "draft": {"tok_s": round(B * gamma / (draft_ms * 1e-3), 1), "ms_per_phase": round(draft_ms, 4),
                   "achieved_gbs": round(draft_gbs, 1), "roofline_frac": round(draft_gbs / peak, 4),
                   "bytes_per_phase": int(pb["draft"]),
                   "calibrate_ms_per_phase": round(calib_ms, 4),
-                  "fuzzy": {"tok_s": round((gamma - 1) / (fuzzy_ms * 1e-3), 1),
+                  "fuzzy": {"tok_s": round(B * (gamma - 1) / (fuzzy_ms * 1e-3), 1),
                             "ms_per_phase": round(fuzzy_ms, 4), "achieved_gbs": round(fuzzy_gbs, 1),
                             "roofline_frac": round(fuzzy_gbs / peak, 4),
                             "bytes_per_phase": int(pb["fuzzy"])}},
