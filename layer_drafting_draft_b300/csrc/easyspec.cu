@@ -56,6 +56,7 @@ struct Rec {
     std::shared_ptr<GvLaunch> host;         // host copy while the plan is built
     std::shared_ptr<GvLaunch> gemm_ops;     // many-row passes: the ops, kept on the host
     bool bf16 = false;                      // weights are bf16
+    int nw = 8;                             // tensor-core weight pass: warps per CTA (8 or 16)
     int grid = 0, smem = 0, M = 0, ntiles64 = 0;
     NormArgs norm{};
     AttnArgs attn{};
@@ -394,10 +395,8 @@ struct GvBuild {
 Rec finish_gv(es_ctx* c, GvBuild& b, const char* name) {
     GvLaunch& L = *b.L;
     // chunk columns and tile rows: 512-byte x 32-row stages (SIMT-FMA kernel)
-    // or 128-column x 128-row stages (tensor-core kernel)
+    // or 128-column x (16 x warps)-row stages (tensor-core kernel)
     const int SC = b.mma ? GVM_COLS : GV_ROW_BYTES / (int)b.esz;
-    const int RT = b.mma ? GVM_BLOCK : GV_RT;
-    int t = 0, st = 0, t64 = 0;
     double wbytes = 0, rowbytes = 0;
     for (int i = 0; i < L.nops; ++i) {
         GvOp& o = L.ops[i];
@@ -408,42 +407,75 @@ Rec finish_gv(es_ctx* c, GvBuild& b, const char* name) {
             o.spt += sg.nck;
             wbytes += (double)o.N * sg.K * b.esz;
         }
-        o.ntiles = (o.N + RT - 1) / RT;
-        o.tile0 = t; o.stage0 = st; o.tile64_0 = t64;
-        t += o.ntiles; st += o.ntiles * o.spt; t64 += (o.N + GB - 1) / GB;
         rowbytes += (double)o.N * 4.0 * (o.epi == GEPI_STORE || o.epi == GEPI_SWIGLU ? 1 : o.epi == GEPI_ACC ? 2 : 3);
     }
     for (int i = 0; i < L.nxs; ++i) rowbytes += (double)L.xs[i].K * 4.0;
-    L.ntiles = t; L.nstages = st; L.ntiles64 = t64;
-    const int ctas = c->num_sms * GV_CTAS_PER_SM;
-    L.q = std::max(1, (st + ctas - 1) / ctas);
-    L.x_smem_floats = b.mma ? GV_XSMEM_MAX : b.xfloats;
+    // tiles and stages for a tile height; the CTA range per `ctas`
+    auto layout = [&](int RT, int ctas) {
+        int t = 0, st = 0, t64 = 0;
+        for (int i = 0; i < L.nops; ++i) {
+            GvOp& o = L.ops[i];
+            o.ntiles = (o.N + RT - 1) / RT;
+            o.tile0 = t; o.stage0 = st; o.tile64_0 = t64;
+            t += o.ntiles; st += o.ntiles * o.spt; t64 += (o.N + GB - 1) / GB;
+        }
+        L.ntiles = t; L.nstages = st; L.ntiles64 = t64;
+        L.q = std::max(1, (st + ctas - 1) / ctas);
+        if (t > GV_COUNTERS) arg_fail(ES_ERR_ARG, "launch has %d tiles (> %d)", t, GV_COUNTERS);
+    };
+    // tensor-core kernel: the largest staged window set of any CTA within
+    // `budget` words (the device repeats this computation with the result
+    // as its budget); false if some window would go through L2
+    auto windows_fit = [&](int budget, int* need) {
+        const int grid = (L.nstages + L.q - 1) / L.q;
+        bool all = true;
+        *need = 0;
+        for (int cta = 0; cta < grid; ++cta) {
+            GvmWin win[GVM_NWIN];
+            int items, used;
+            const int n = gvm_windows(L, cta * L.q, std::min(L.nstages, (cta + 1) * L.q), win, budget, &items,
+                                      &used);
+            *need = std::max(*need, used);
+            if (n == GVM_NWIN) all = false;  // windows may have been dropped
+            for (int i = 0; i < n; ++i) all = all && win[i].off >= 0;
+        }
+        return all;
+    };
+    Rec r;
+    r.nw = GV_WARPS;
+    if (b.mma) {
+        int need = 0;
+        layout(GVM_BLOCK, c->num_sms * GV_CTAS_PER_SM);
+        if (!windows_fit(GV_XSMEM_MAX, &need)) {
+            // wide activations: one 16-warp CTA per SM shares a window twice
+            // as large, if that makes every window fit
+            int need_w = 0;
+            layout(GVM_WIDE_WARPS * GVM_ROWS, c->num_sms);
+            if (windows_fit(GVM_WIDE_XSMEM, &need_w)) {
+                r.nw = GVM_WIDE_WARPS;
+                need = need_w;
+            } else {
+                layout(GVM_BLOCK, c->num_sms * GV_CTAS_PER_SM);
+                windows_fit(GV_XSMEM_MAX, &need);
+            }
+        }
+        L.x_smem_floats = need;
+    } else {
+        layout(GV_RT, c->num_sms * GV_CTAS_PER_SM);
+        L.x_smem_floats = b.xfloats;
+    }
     int items = 0;  // staging items (4 columns of one row) of the shared-memory sources
     for (int i = 0; i < L.nxs; ++i) {
         L.xs[i].item0 = items;
         if (!b.mma && L.xs[i].smem_off >= 0) items += L.M * (L.xs[i].K / 4);
     }
     L.x_items = items;
-    if (t > GV_COUNTERS) arg_fail(ES_ERR_ARG, "launch has %d tiles (> %d)", t, GV_COUNTERS);
-    Rec r;
     r.kind = b.simt ? R_GEMM : R_GV;
     r.name = name;
     r.M = L.M;
-    r.grid = (st + L.q - 1) / L.q;
-    if (b.mma) {
-        // shared memory: the largest staged window set of any CTA (the device
-        // repeats this computation with the result as its budget)
-        int need = 0;
-        for (int cta = 0; cta < r.grid; ++cta) {
-            GvmWin win[GVM_NWIN];
-            int items, used;
-            gvm_windows(L, cta * L.q, std::min(st, (cta + 1) * L.q), win, GV_XSMEM_MAX, &items, &used);
-            need = std::max(need, used);
-        }
-        L.x_smem_floats = need;
-    }
+    r.grid = (L.nstages + L.q - 1) / L.q;
     r.smem = L.x_smem_floats * (int)sizeof(float);
-    r.ntiles64 = t64;
+    r.ntiles64 = L.ntiles64;
     r.bytes = wbytes + L.M * rowbytes;
     r.host = b.L;
     return r;
@@ -742,8 +774,12 @@ void run_rec(es_ctx* c, const Rec& r) {
     switch (r.kind) {
         case R_GV:
             if constexpr (std::is_same<T, bf16>::value) {
-                launch(c, r.name, r.bytes, gvm_kernel, dim3(r.grid), dim3(GV_THREADS), (size_t)r.smem, r.gv,
-                       c->gv_scratch, c->gv_counters, c->gv_done);
+                if (r.nw == GVM_WIDE_WARPS)
+                    launch(c, r.name, r.bytes, gvm_kernel<GVM_WIDE_WARPS>, dim3(r.grid), dim3(GVM_WIDE_WARPS * 32),
+                           (size_t)r.smem, r.gv, c->gv_scratch, c->gv_counters, c->gv_done);
+                else
+                    launch(c, r.name, r.bytes, gvm_kernel<GV_WARPS>, dim3(r.grid), dim3(GV_THREADS), (size_t)r.smem,
+                           r.gv, c->gv_scratch, c->gv_counters, c->gv_done);
             } else {
                 switch (r.M) {
 #define ES_GV_CASE(MM)                                                                              \
@@ -1285,7 +1321,9 @@ es_status easyspec_init(const es_config* cfg, const es_weights* draft, const es_
         ES_GV_ATTR(float, 1) ES_GV_ATTR(float, 2) ES_GV_ATTR(float, 3) ES_GV_ATTR(float, 4)
         ES_GV_ATTR(float, 5) ES_GV_ATTR(float, 6) ES_GV_ATTR(float, 7) ES_GV_ATTR(float, 8)
 #undef ES_GV_ATTR
-        CK(cudaFuncSetAttribute(gvm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, gv_smem));
+        CK(cudaFuncSetAttribute(gvm_kernel<GV_WARPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, gv_smem));
+        CK(cudaFuncSetAttribute(gvm_kernel<GVM_WIDE_WARPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                GVM_WIDE_XSMEM * (int)sizeof(float)));
         const int att_smem = 200 * 1024;
         CK(cudaFuncSetAttribute(attn_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, att_smem));
         CK(cudaFuncSetAttribute(attn_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, att_smem));

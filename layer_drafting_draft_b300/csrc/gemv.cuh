@@ -553,7 +553,12 @@ gv_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __r
 // launch's shared memory to its largest window set: a larger request would
 // shrink the L1 that the streaming loads pass through.
 constexpr int GVM_ROWS = 16;                     // rows per warp
-constexpr int GVM_BLOCK = GVM_ROWS * GV_WARPS;   // rows per stage (128)
+constexpr int GVM_BLOCK = GVM_ROWS * GV_WARPS;   // rows per stage (128) of the 8-warp variant
+// The 16-warp variant (one 512-thread CTA per SM, 256-row stages) shares one
+// activation window between twice the warps: for widths whose windows do
+// not fit the 8-warp budget.
+constexpr int GVM_WIDE_WARPS = 16;
+constexpr int GVM_WIDE_XSMEM = 48 * 1024;        // 4-byte words (192 KB)
 constexpr int GVM_COLS = 128;                    // columns per stage
 constexpr int GVM_D = 2;                         // stages in flight per warp
 constexpr int GVM_NWIN = 16;                     // activation windows per CTA
@@ -665,7 +670,7 @@ __host__ __device__ inline int gvm_windows(const GvLaunch& L, int S0, int S1, Gv
 }
 
 // Stage the windows with off >= 0 as hi/lo planes (whole CTA; synchronises).
-template <int SB>  // items per thread with their loads in flight together
+template <int SB, int NT>  // items per thread with their loads in flight together; threads
 ES_DEV void gvm_stage(const GvLaunch& L, const GvmWin* win, int nwin, int nitems, unsigned char* xsm,
                       const float* srinv) {
     const int M = L.M;
@@ -677,11 +682,11 @@ ES_DEV void gvm_stage(const GvLaunch& L, const GvmWin* win, int nwin, int nitems
         m = r / C4;
         kr = (r - m * C4) * 4;
     };
-    for (int t0 = threadIdx.x; t0 < nitems; t0 += SB * GV_THREADS) {
+    for (int t0 = threadIdx.x; t0 < nitems; t0 += SB * NT) {
         float4 v[SB];
 #pragma unroll
         for (int u = 0; u < SB; ++u) {
-            const int t = t0 + u * GV_THREADS;
+            const int t = t0 + u * NT;
             v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (t < nitems) {
                 int i, m, kr;
@@ -693,7 +698,7 @@ ES_DEV void gvm_stage(const GvLaunch& L, const GvmWin* win, int nwin, int nitems
         }
 #pragma unroll
         for (int u = 0; u < SB; ++u) {
-            const int t = t0 + u * GV_THREADS;
+            const int t = t0 + u * NT;
             if (t >= nitems) break;
             int i, m, kr;
             locate(t, i, m, kr);
@@ -762,12 +767,13 @@ struct GvmIssue {
     int kc, kc_end;
 };
 
+template <int NW>
 ES_DEV void gvm_issue_begin(const GvLaunch& L, GvmWarp& ws, GvmIssue& I, int s_end) {
     const GvmRun r = gvm_next_run(L, ws.ip, ws.is, s_end);
     const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
     const GvOp& o = L.ops[r.op];
     const GvSeg& sg = L.segs[o.seg0 + r.seg];
-    const int w0 = r.tile * GVM_BLOCK + (threadIdx.x >> 5) * GVM_ROWS;
+    const int w0 = r.tile * (NW * GVM_ROWS) + (threadIdx.x >> 5) * GVM_ROWS;
     // rows past N read the last row (their sums are dropped); warps wholly
     // past N load nothing
     I.ra = (const bf16*)sg.W + (size_t)min(w0 + g, o.N - 1) * sg.K + 8 * c;
@@ -781,6 +787,7 @@ ES_DEV void gvm_issue_begin(const GvLaunch& L, GvmWarp& ws, GvmIssue& I, int s_e
 // Whole chunks take unpredicated loads; only a segment's ragged last chunk
 // (or a warp past N) checks columns.  (A bulk L2 prefetch of the chunk 4 or
 // 8 stages ahead measured slower: 223 and 219 against 236 tok/s.)
+template <int NW>
 ES_DEV void gvm_issue_step(const GvLaunch& L, GvmWarp& ws, GvmIssue& I, GvmStage& st, int s_end) {
     const int kb = I.kc * GVM_COLS;
     const bf16* pa = I.ra + kb;
@@ -800,7 +807,7 @@ ES_DEV void gvm_issue_step(const GvLaunch& L, GvmWarp& ws, GvmIssue& I, GvmStage
             st.b[j] = in ? ld_stream16(pb + 32 * j) : make_uint4(0u, 0u, 0u, 0u);
         }
     }
-    if (++I.kc == I.kc_end && ws.is < s_end) gvm_issue_begin(L, ws, I, s_end);
+    if (++I.kc == I.kc_end && ws.is < s_end) gvm_issue_begin<NW>(L, ws, I, s_end);
 }
 
 // Consume side: the activation operand of the current run.
@@ -989,13 +996,14 @@ ES_DEV void gvm_rinv_finish(const GvLaunch& L, const GvmRinv& R, float* srinv) {
 }
 
 
-__global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM)
+template <int NW>
+__global__ void __launch_bounds__(NW * 32, NW == GV_WARPS ? GV_CTAS_PER_SM : 1)
 gvm_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __restrict__ counters,
            int* __restrict__ done) {
     extern __shared__ __align__(16) unsigned char gvm_xsm[];
     __shared__ __align__(16) GvLaunch L;
     __shared__ GvmWin win[GVM_NWIN];
-    __shared__ GvmWarp wstate[GV_WARPS];
+    __shared__ GvmWarp wstate[NW];
     __shared__ float srinv[GV_MAXM];
     __shared__ int s_nwin, s_items, s_last, s_done;
     gv_load_desc(L, Lg);
@@ -1014,22 +1022,22 @@ gvm_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __
     int s_issue = S0;
     ws.ip = ws.cp = gvm_seek(L, S0);
     ws.is = ws.cs = S0;
-    gvm_issue_begin(L, ws, I, S1);
+    gvm_issue_begin<NW>(L, ws, I, S1);
 #pragma unroll
     for (int i = 0; i < GVM_D - 1; ++i)
-        if (s_issue < S1) { gvm_issue_step(L, ws, I, ring[i], S1); ++s_issue; }
+        if (s_issue < S1) { gvm_issue_step<NW>(L, ws, I, ring[i], S1); ++s_issue; }
     __syncthreads();
     grid_dep_wait();
     grid_dep_launch();
     // the ring's other stage goes out before the staging round trips
 #pragma unroll
     for (int i = GVM_D - 1; i < GVM_D; ++i)
-        if (s_issue < S1) { gvm_issue_step(L, ws, I, ring[i], S1); ++s_issue; }
+        if (s_issue < S1) { gvm_issue_step<NW>(L, ws, I, ring[i], S1); ++s_issue; }
     const int nwin = s_nwin;
     {
         GvmRinv R;
         gvm_rinv_issue(L, R);
-        gvm_stage<8>(L, win, nwin, s_items, gvm_xsm, srinv);  // ends with a barrier
+        gvm_stage<8, NW * 32>(L, win, nwin, s_items, gvm_xsm, srinv);  // ends with a barrier
         gvm_rinv_finish(L, R, srinv);
         __syncthreads();
     }
@@ -1047,7 +1055,7 @@ gvm_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __
             else gvm_cons_step(L, ws, C, ring[i], acc1, srinv);
             // refill the slot just multiplied: GVM_D stages stay in flight
             if (s_issue < S1) {
-                gvm_issue_step(L, ws, I, ring[i], S1);
+                gvm_issue_step<NW>(L, ws, I, ring[i], S1);
                 ++s_issue;
             }
             if (C.kc < C.kc_end) continue;
@@ -1059,7 +1067,7 @@ gvm_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __
                 bool do_epi = blk_first >= S0 && blk_last < S1;
                 if (!do_epi) {
                     const int sid = S0 >= blk_first ? 0 : 1;
-                    float* part = scratch + ((size_t)((cta * 2 + sid) * GV_WARPS + warp) * 2) * 128 + lane * 4;
+                    float* part = scratch + ((size_t)((cta * 2 + sid) * NW + warp) * 2) * 128 + lane * 4;
                     *reinterpret_cast<float4*>(part) = make_float4(acc0[0], acc0[1], acc0[2], acc0[3]);
                     if (two) *reinterpret_cast<float4*>(part + 128) = make_float4(acc1[0], acc1[1], acc1[2], acc1[3]);
                     __syncthreads();
@@ -1085,7 +1093,7 @@ gvm_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __
                                     if (cc <= c_last) {
                                         const int sd = cc * q >= blk_first ? 0 : 1;
                                         pv[u] = __ldcg(reinterpret_cast<const float4*>(
-                                            scratch + ((size_t)((cc * 2 + sd) * GV_WARPS + warp) * 2 + set) * 128 +
+                                            scratch + ((size_t)((cc * 2 + sd) * NW + warp) * 2 + set) * 128 +
                                             lane * 4));
                                     }
                                 }
@@ -1107,7 +1115,7 @@ gvm_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __
                     __syncthreads();
                 }
                 if (do_epi)
-                    gvm_epilogue(L, o, ws.tile * GVM_BLOCK + warp * GVM_ROWS, acc0, acc1,
+                    gvm_epilogue(L, o, ws.tile * (NW * GVM_ROWS) + warp * GVM_ROWS, acc0, acc1,
                                  L.post.ssp != nullptr && ws.op == L.post.op, srinv);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc0[e] = acc1[e] = 0.f;
@@ -1116,7 +1124,9 @@ gvm_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __
             if (si + 1 < S1) gvm_cons_begin(L, ws, C, win, nwin, gvm_xsm, S1);
         }
     }
-    if (L.post.rows > 0 && !L.post.ssp) {
+    // (the last-CTA norm pass is sized for 8-warp CTAs; bf16 launches pass
+    // sums of squares instead)
+    if (NW == GV_WARPS && L.post.rows > 0 && !L.post.ssp) {
         __syncthreads();
         const int old = cta_arrive(done);
         if (tid == 0) s_done = old == (int)gridDim.x - 1;

@@ -71,3 +71,37 @@ def test_fullwidth_logits_within_tolerance():
     assert worst["q"] <= BF16_MAXABS and worst["p"] <= BF16_MAXABS
     assert worst["rel"] <= BF16_RELL2
     g.close()
+
+
+def test_wide_window_variant_within_tolerance():
+    """A base of d 4096 and ffn 20480 verified over gamma+1 = 8 rows.
+
+    The gate/up pass's activation window (8 rows x 4096 columns as hi/lo
+    planes) does not fit the 8-warp budget. The planner therefore takes the
+    16-warp variant for it, one 512-thread CTA per SM, as it does at the
+    Llama-3-70B widths. Logits must meet the bf16 tolerance against the
+    oracle.
+    """
+    d = synth.shape(4, 256, 4, 2, 688, 1000, 1e4)
+    b = synth.shape(2, 4096, 32, 8, 20480, 1000, 5e5)
+    pair = Pair(d, b, "bf16", 23)
+    gamma = 7
+    prompt = synth.make_prompts(1, 20, 1000, 24).numpy()
+    g = pair.gpu(max_seq=128, max_gamma=8, mode=ES_FULL_LAYER)
+    o = pair.oracle(k=2, mode=ES_FULL_LAYER, max_len=128)
+    g.easyspec_prefill(prompt)
+    o.prefill(prompt.tolist())
+    worst, rel = 0.0, 0.0
+    for ph in range(2):
+        d_gpu = g.draft_step(2, gamma, 0.0, 41 + ph)
+        o.draft_row(0, gamma, 0.0, 41 + ph, force_d=d_gpu[0])
+        n, toks = g.verify_step(0.0, 41 + ph, gamma)
+        a = int(n[0])
+        o.verify_row(0, gamma, 0.0, 41 + ph, force=(a, toks[0, : a + 1]))
+        zp = g.es_read_dist(3, gamma)[0]
+        zp_or = np.asarray(o.rows[0].zp, np.float64)
+        worst = max(worst, float(np.max(np.abs(zp - zp_or))))
+        rel = max(rel, rel_l2(zp, zp_or))
+    print("wide-window bf16:", worst, rel)
+    assert worst <= BF16_MAXABS and rel <= BF16_RELL2
+    g.close()
