@@ -1,7 +1,7 @@
 """Run speculative phases of a synthetic workload for profiling.
 
     python -m layer_drafting_draft_b300.profile --workload qwen2.5_0.5b_7b_bf16 \
-        --k 4 --phases 4 --warmup-phases 2 [--table] [--base-layers N]
+        --k 4 --phases 4 --warmup-phases 2 [--table] [--base-layers N] [--batch B]
 
 After the prompt prefill and `--warmup-phases` untimed phases, `--phases`
 phases (draft_step + verify_step) run inside the NVTX range "measure", so an
@@ -35,6 +35,7 @@ def main(argv=None):
     ap.add_argument("--warmup-phases", type=int, default=2)
     ap.add_argument("--base-layers", type=int, default=None)
     ap.add_argument("--draft-layers", type=int, default=None)
+    ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--table", action="store_true")
     a = ap.parse_args(argv)
 
@@ -48,13 +49,13 @@ def main(argv=None):
     seed = 1000 * wl["seed"]
     wb = synth.make_weights(sb, seed + 2, wl["dtype"], "cuda")
     wd = synth.make_weights(sd, seed + 1, wl["dtype"], "cuda")
-    prompt = synth.make_prompts(1, wl["prompt"], sb["vocab"], seed + 3).numpy()
+    prompt = synth.make_prompts(a.batch, wl["prompt"], sb["vocab"], seed + 3).numpy()
     gamma = a.gamma or wl["gamma"]
     k = a.k if sd["n_layers"] > 2 else 1
     n_ph = a.warmup_phases + a.phases
     max_seq = (wl["prompt"] + 2 * (n_ph + 1) * (gamma + 1) + 63) // 64 * 64
     stream = torch.cuda.Stream()
-    g = EasySpec(wd, sd, wb, sb, wl["dtype"], 1, max_seq, gamma,
+    g = EasySpec(wd, sd, wb, sb, wl["dtype"], a.batch, max_seq, gamma,
                  ES_FULL_LAYER if a.mode == "full" else ES_ATTN_ONLY, None, stream)
 
     def phases(n, s0):
