@@ -31,6 +31,12 @@ Readings (the pages leave these steps open; see also the design notes):
   * The prompt's base prefill covers x_0..x_{P-2}; the draft's prompt
     prefill is the first calibration.
   * Every phase drafts a full gamma; the output is cut to max_new at the end.
+  * Calibration ablation (``calibrate=False``; the pages' ablation says that
+    without calibration the fuzzy errors accumulate): after acceptance of a
+    drafts the accepted drafts that carried a fuzzy entry (d_1..d_min(a,
+    gamma-1)) keep it. Only the positions that have no entry, the bonus y
+    and, when every draft was accepted, d_gamma, go through the exact draft
+    forward that starts the next phase.
 """
 from __future__ import annotations
 
@@ -70,7 +76,7 @@ class SpecDecoder:
 
     def __init__(self, Wd, shape_d: M.Shape, Wb, shape_b: M.Shape,
                  groups=None, k: int = 1, mode: int = M.FULL_LAYER,
-                 max_len: int = 256):
+                 max_len: int = 256, calibrate: bool = True):
         if shape_d.vocab != shape_b.vocab:
             raise ValueError("draft and base must share one vocabulary")
         self.Wd, self.sd, self.Wb, self.sb = Wd, shape_d, Wb, shape_b
@@ -78,6 +84,7 @@ class SpecDecoder:
         M.check_groups(self.groups, shape_d.n_layers)
         self.mode = mode
         self.max_len = max_len
+        self.calibrate = calibrate
         self.rows: list[Row] = []
 
     # -------------------------------------------------------------- stages
@@ -141,7 +148,9 @@ class SpecDecoder:
             a, new = int(force[0]), [int(t) for t in force[1]]
         r.n_acc = a
         r.tokens += new
-        r.draft_len = n
+        # calibration recomputes every committed position from n on; without
+        # it the fuzzy entries of the accepted d_1..d_min(a, gamma-1) stay
+        r.draft_len = n if self.calibrate else n + min(a, gamma - 1)
         r.phase += 1
         return a, new
 

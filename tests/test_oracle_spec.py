@@ -149,3 +149,81 @@ def test_sampled_output_follows_base_distribution(mode):
     ex = np.append(exp[keep], exp[~keep].sum())
     chi = stats.chisquare(obs, ex * obs.sum() / ex.sum())
     assert chi.pvalue > 1e-3, (chi, counts, exp)
+
+
+# ------------------------------------------------ calibration ablation
+# Without calibration the accepted drafts keep the entries their layer-parallel
+# forwards wrote (the pages' ablation: the fuzzy errors then accumulate). The
+# rule itself fixes three checkable facts.
+
+@pytest.mark.parametrize("k,mode", [(2, M.FULL_LAYER), (3, M.ATTN_ONLY)])
+def test_no_calibration_greedy_still_lossless(k, mode):
+    # losslessness does not depend on the draft's cache
+    Wd, sd, Wb, sb = tiny_pair(10, std=0.3, Ld=5)
+    prompts = [[5, 6, 7, 8], [60, 1, 2]]
+    want = [spec.seq_decode(Wb, sb, p, 20, 64) for p in prompts]
+    dec = spec.SpecDecoder(Wd, sd, Wb, sb, k=k, mode=mode, max_len=64, calibrate=False)
+    assert dec.generate(prompts, 20, 4, 0.0) == want
+
+
+@pytest.mark.parametrize("temp", [0.0, 1.0])
+def test_no_calibration_with_exact_drafts_changes_nothing(temp):
+    # with one-layer sets every draft forward is exact, so the kept entries
+    # are the calibrated ones: tokens and draft logits must be identical.
+    # A self-draft pair makes every draft accepted often, which exercises the
+    # d_gamma row (no entry of its own) of the narrowed calibration window.
+    _, _, Wb, sb = tiny_pair(11, std=0.3)
+    Wd = _perturbed(Wb, 0.02, 1)
+    runs = {}
+    for cal in (True, False):
+        dec = spec.SpecDecoder(Wd, sb, Wb, sb, k=1, max_len=96, calibrate=cal)
+        dec.prefill([[3, 1, 4, 1, 5]])
+        zq, acc = [], []
+        for _ in range(8):
+            dec.draft_row(0, 4, temp, 7)
+            zq.append(dec.rows[0].zq.copy())
+            acc.append(dec.verify_row(0, 4, temp, 7)[0])
+        runs[cal] = (dec.rows[0].tokens, zq, acc)
+    assert 4 in runs[True][2]
+    assert runs[True][0] == runs[False][0]
+    assert all(np.array_equal(a, b) for a, b in zip(runs[True][1], runs[False][1]))
+
+
+@pytest.mark.parametrize("mode", [M.FULL_LAYER, M.ATTN_ONLY])
+def test_no_calibration_cache_keeps_accepted_fuzzy_entries(mode):
+    # Replay the committed tokens position by position, taking the layer-
+    # parallel forward exactly at the positions whose drafts were accepted and
+    # had been draft inputs (d_1..d_min(a, gamma-1) of each phase), the exact
+    # one elsewhere. Each forward reads only earlier positions, so the replay
+    # must reproduce the draft cache bit for bit.
+    _, _, Wb, sb = tiny_pair(15, std=0.3, Lb=6)
+    Wd = _perturbed(Wb, 0.02, 2)
+    gamma = 4
+    dec = spec.SpecDecoder(Wd, sb, Wb, sb, k=2, mode=mode, max_len=96, calibrate=False)
+    assert any(len(g) > 1 for g in dec.groups)
+    dec.prefill([[2, 7, 1, 8]])
+    r = dec.rows[0]
+    fuzzy_pos, accepted = set(), []
+    for _ in range(8):
+        n = len(r.tokens)
+        dec.draft_row(0, gamma, 0.0, 3)
+        a, _ = dec.verify_row(0, gamma, 0.0, 3)
+        accepted.append(a)
+        fuzzy_pos.update(range(n, n + min(a, gamma - 1)))
+    dec.draft_row(0, gamma, 0.0, 3)   # the narrowed calibration of the last commits
+    n = r.draft_len
+    assert n == len(r.tokens) and len(fuzzy_pos) >= 3, accepted
+    replay = M.KVCache(sb, 96)
+    for pos, t in enumerate(r.tokens[:n]):
+        if pos in fuzzy_pos:
+            M.forward_fuzzy(Wd, sb, t, pos, replay, dec.groups, mode)
+        else:
+            M.forward_exact(Wd, sb, t, pos, replay)
+    assert np.array_equal(r.draft.K[:, :n], replay.K[:, :n])
+    assert np.array_equal(r.draft.V[:, :n], replay.V[:, :n])
+    # and the kept entries are not the exact ones
+    exact = M.KVCache(sb, 96)
+    for pos, t in enumerate(r.tokens[:n]):
+        M.forward_exact(Wd, sb, t, pos, exact)
+    p = min(fuzzy_pos)
+    assert not np.allclose(r.draft.K[:, p], exact.K[:, p])
