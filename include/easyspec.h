@@ -141,6 +141,18 @@ ES_API es_status easyspec_prefill(es_ctx *ctx, const int32_t *prompts, int B, in
  * gamma as in draft_step; temperature 0 = greedy. */
 ES_API es_status calibrate_kv(es_ctx *ctx, int gamma, float temperature, uint64_t seed);
 
+/* Calibration ablation ([ABS]; [DISC] first reply: without calibration the
+ * fuzzy errors accumulate).  on = 1 (the default after easyspec_init) runs
+ * the calibration above.  on = 0 keeps, after each verify_step, the
+ * layer-parallel KV entries of the accepted drafts d_1..d_min(a, gamma-1);
+ * the exact draft forward that starts the next phase then covers only the
+ * committed positions that hold no draft entry (the bonus token, and d_gamma
+ * when every draft was accepted) and still yields q_1.  Takes effect at the
+ * next calibrate_kv / draft_step / es_decode / generate; the positions kept
+ * so far stay as they are.  ES_ERR_ARG unless on is 0 or 1; ES_ERR_STATE
+ * between a draft_step (or calibrate_kv) and its verify_step. */
+ES_API es_status es_set_calibration(es_ctx *ctx, int on);
+
 /* Drafting ([ABS]; [DISC] Table 4 and Figure 2 replies): calibration (if
  * pending) then gamma-1 layer-parallel draft forwards of d_1..d_{gamma-1}
  * under layer-set size k (ignored, and must be 0, when explicit sets were

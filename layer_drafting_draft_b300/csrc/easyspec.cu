@@ -113,6 +113,7 @@ struct es_ctx {
     // device state
     int* tokens = nullptr;   // [Bmax][max_seq]
     int* n_commit = nullptr; // [Bmax]
+    int* kv_from = nullptr;  // [Bmax] first committed position without a draft K/V entry
     int* n_limit = nullptr;  // [Bmax] commit limit (generate: P + max_new)
     int64_t* phase = nullptr;
     int* dtok = nullptr;     // [Bmax][gmax]
@@ -143,6 +144,7 @@ struct es_ctx {
     std::vector<int> n_host;  // committed count per sequence (host copy)
     int cur_gamma = 0, cur_k = -1;
     bool calibrated = false, drafted = false;
+    bool calib_off = false;  // calibration ablation
     float cur_T = 0.f;
     uint64_t cur_seed = 0;
 
@@ -817,7 +819,7 @@ EmbedArgs embed_args(es_ctx* c, Model& m, const Plan& plan, int kind, int step, 
     e.kind = kind; e.step = step; e.gamma = gamma; e.M = M;
     e.n_commit = c->n_commit; e.tokens = c->tokens; e.max_seq = c->cfg.max_seq; e.dtok = c->dtok;
     e.gmax = c->cfg.max_gamma; e.row_pos = m.row_pos; e.row_seq = m.row_seq; e.row_tok = m.row_tok;
-    e.row_base = m.row_base; e.E = m.embed; e.h = m.h; e.d = m.d; e.V = m.V; e.status = c->status;
+    e.row_base = m.row_base; e.kv_from = c->kv_from; e.prm = c->prm; e.E = m.embed; e.h = m.h; e.d = m.d; e.V = m.V; e.status = c->status;
     e.post = plan.first;
     return e;
 }
@@ -960,13 +962,14 @@ void enqueue_verify(es_ctx* c, int gamma) {
     vocab_chunks(m.V, c->num_sms, &a.chunk, &a.nb);
     a.gpart = c->sm_part; a.mass = c->sm_mass; a.counters = c->sm_counters;
     a.n_acc = c->n_acc; a.out_tok = c->out_tok; a.tokens = c->tokens; a.max_seq = c->cfg.max_seq;
-    a.n_commit = c->n_commit; a.n_limit = c->n_limit;
+    a.n_commit = c->n_commit; a.n_limit = c->n_limit; a.kv_from = c->kv_from;
     launch(c, "accept_resample", 0.0, accept_kernel, dim3(B, a.nb), dim3(SM_THREADS), (size_t)0, a);
 }
 
 void set_params(es_ctx* c, float T, uint64_t seed) {
     c->h_prm->seed = seed;
     c->h_prm->temperature = T;
+    c->h_prm->calib_off = c->calib_off ? 1 : 0;
     CK(cudaMemcpyAsync(c->prm, c->h_prm, sizeof(RunParams), cudaMemcpyHostToDevice, c->st));
 }
 
@@ -1089,8 +1092,10 @@ void do_prefill(es_ctx* c, const int32_t* prompts, int B, int P) {
     for (int b = 0; b < B; ++b)
         CK(cudaMemcpyAsync(c->tokens + (size_t)b * c->cfg.max_seq, prompts + (size_t)b * P,
                            P * sizeof(int), cudaMemcpyHostToDevice, c->st));
-    std::vector<int> n(B, P), lim(B, 0x7fffffff);
+    std::vector<int> n(B, P), lim(B, 0x7fffffff), kv(B, P - 1);
     CK(cudaMemcpyAsync(c->n_commit, n.data(), B * sizeof(int), cudaMemcpyHostToDevice, c->st));
+    // the draft's prompt prefill below computes positions 0..P-2 exactly
+    CK(cudaMemcpyAsync(c->kv_from, kv.data(), B * sizeof(int), cudaMemcpyHostToDevice, c->st));
     CK(cudaMemcpyAsync(c->n_limit, lim.data(), B * sizeof(int), cudaMemcpyHostToDevice, c->st));
     CK(cudaMemsetAsync(c->phase, 0, sizeof(int64_t) * c->cfg.max_batch, c->st));
     c->n_host.assign(B, P);
@@ -1273,6 +1278,7 @@ es_status easyspec_init(const es_config* cfg, const es_weights* draft, const es_
         const int Bm = cfg->max_batch, S = cfg->max_seq, G = cfg->max_gamma, V = cfg->draft.vocab;
         c->tokens = c->dalloc<int>((size_t)Bm * S);
         c->n_commit = c->dalloc<int>(Bm);
+        c->kv_from = c->dalloc<int>(Bm);
         c->n_limit = c->dalloc<int>(Bm);
         c->phase = c->dalloc<int64_t>(Bm);
         c->dtok = c->dalloc<int>((size_t)Bm * G);
@@ -1343,6 +1349,16 @@ es_status easyspec_init(const es_config* cfg, const es_weights* draft, const es_
 es_status easyspec_prefill(es_ctx* c, const int32_t* prompts, int B, int P) {
     if (!c) return ES_ERR_ARG;
     return guarded(c, [&] { do_prefill(c, prompts, B, P); });
+}
+
+es_status es_set_calibration(es_ctx* c, int on) {
+    if (!c) return ES_ERR_ARG;
+    return guarded(c, [&] {
+        if (on != 0 && on != 1) arg_fail(ES_ERR_ARG, "es_set_calibration: on must be 0 or 1");
+        if (c->calibrated || c->drafted)
+            arg_fail(ES_ERR_STATE, "es_set_calibration: a phase is in progress (finish it with verify_step)");
+        c->calib_off = on == 0;
+    });
 }
 
 es_status calibrate_kv(es_ctx* c, int gamma, float temperature, uint64_t seed) {

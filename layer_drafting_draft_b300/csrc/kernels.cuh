@@ -21,7 +21,10 @@ enum { KIND_HOST = 0, KIND_CALIB = 1, KIND_FUZZY = 2, KIND_VERIFY = 3 };
 // KIND_CALIB : rows (b, i), i = 0..gamma: position n_b - gamma - 1 + i (the
 //              last gamma+1 committed tokens; recomputing already-exact
 //              positions reproduces their entries, so the window always covers
-//              every pending token)
+//              every pending token).  Under the calibration ablation
+//              (prm->calib_off) rows before kv_from[b] are inactive: the
+//              accepted drafts keep their layer-parallel entries and only the
+//              positions without one are computed.
 // KIND_FUZZY : rows b, position n_b + step - 1, token d[b][step-1]
 // KIND_VERIFY: rows (b, j), j = 0..gamma: position n_b - 1 + j, token
 //              x_{n_b-1} for j = 0, d[b][j-1] otherwise
@@ -32,6 +35,7 @@ struct EmbedArgs {
     int kind, step, gamma, M;
     const int* n_commit; const int* tokens; int max_seq; const int* dtok; int gmax;
     int* row_pos; int* row_seq; int* row_tok; int* row_base;
+    const int* kv_from; const RunParams* prm;  // calibration ablation (KIND_CALIB)
     const void* E; float* h; int d, V;
     int* status;
     GvPost post;  // 1/rms of the embedded rows (rows map one to one)
@@ -51,11 +55,17 @@ ES_DEV void embed_item(const EmbedArgs& a, int m) {
     } else if (kind == KIND_CALIB) {
         b = m / (gamma + 1);
         const int nb = __ldcg(a.n_commit + b);
-        // first active row of the block (rows before it have no position yet)
-        base = b * (gamma + 1) + max(0, gamma + 1 - nb);
+        // first position the window computes: 0, or kv_from[b] without
+        // calibration (never past the last committed token)
+        int lo = 0;
+        if (a.kv_from && a.prm->calib_off) lo = min(max(__ldcg(a.kv_from + b), 0), nb - 1);
+        // first active row of the block (rows before it have no position
+        // yet, or keep their entries)
+        base = b * (gamma + 1) + max(gamma + 1 - nb, lo - (nb - gamma - 1));
+        base = max(base, b * (gamma + 1));
         const int i = m % (gamma + 1);
         pos = nb - (gamma + 1) + i;
-        if (pos < 0) pos = -1;
+        if (pos < lo) pos = -1;
         tok = (pos >= 0 && pos < max_seq) ? __ldcg(a.tokens + (size_t)b * max_seq + pos) : 0;
     } else if (kind == KIND_FUZZY) {
         b = m;

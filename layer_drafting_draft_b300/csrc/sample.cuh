@@ -21,7 +21,9 @@ namespace es {
 constexpr int SM_THREADS = 256;
 constexpr int SM_COUNTERS = 4096;
 
-struct RunParams { uint64_t seed; float temperature; int pad_; };
+// calib_off: 1 = calibration ablation (the next exact draft forward covers
+// only the positions that hold no draft entry, see the row setup)
+struct RunParams { uint64_t seed; float temperature; int calib_off; };
 
 // Row r of a launch: sequence b = r / per_seq, slot i = r % per_seq + off;
 // its logits / probabilities live at row (b * ld_rows + i) of z / p.
@@ -274,7 +276,8 @@ ES_DEV void softmax_finish_item(const SampleArgs& a, int r, int c) {
 // CTA adds the integer masses of its chunk, the last one locates the draw.
 // The deciding CTA writes n_acc and the tokens and, when `tokens` is set,
 // commits them (n_commit += j + 1 unless the sequence reached n_limit;
-// phase += 1).
+// phase += 1; kv_from = n + min(j, g - 1), the first committed position
+// with no draft K/V entry once the accepted drafts keep theirs).
 struct AcceptArgs {
     const float* p; const float* q; const int* d; int gmax, gamma, V, nb, chunk;
     int greedy;                    // 1 / 0, or -1: greedy when prm->temperature == 0
@@ -285,6 +288,7 @@ struct AcceptArgs {
     int* counters;                 // [B]
     int* n_acc; int* out_tok;      // [B], [B][g+1] (-1 past n_acc+1)
     int* tokens; int max_seq; int* n_commit; const int* n_limit;
+    int* kv_from;                  // [B] or null
 };
 
 // Item (sequence b, chunk c) of accept/resample.  Whole CTA.
@@ -411,6 +415,8 @@ ES_DEV void accept_item(const AcceptArgs& a, int b, int c) {
             if (n + j < a.max_seq) tk[n + j] = y;
             a.n_commit[b] = n + j + 1;
             a.phase[b] = __ldcg(a.phase + b) + 1;
+            // d_1..d_{g-1} were draft inputs at positions n..n+g-2
+            if (a.kv_from) a.kv_from[b] = n + min(j, g - 1);
         }
     }
 }

@@ -23,7 +23,7 @@ ES_ATTN_ONLY, ES_FULL_LAYER = 0, 1
 STATUS_NAMES = {0: "ES_OK", -1: "ES_ERR_ARG", -2: "ES_ERR_OOM", -3: "ES_ERR_CUDA",
                 -4: "ES_ERR_TIMEOUT", -5: "ES_ERR_STATE", -6: "ES_ERR_CAPACITY"}
 
-EXPORTED = ["easyspec_init", "easyspec_prefill", "calibrate_kv", "draft_step", "verify_step",
+EXPORTED = ["easyspec_init", "easyspec_prefill", "calibrate_kv", "es_set_calibration", "draft_step", "verify_step",
             "generate", "es_decode", "es_profile", "es_profile_read", "es_accept_resample",
             "es_accept_resample_noalloc",
             "es_sample", "es_read_kv", "es_read_dist", "es_read_tokens", "easyspec_last_error",
@@ -76,6 +76,7 @@ def lib() -> C.CDLL:
             "easyspec_init": ([C.POINTER(es_config), C.POINTER(es_weights), C.POINTER(es_weights), C.POINTER(C.c_void_p)], C.c_int),
             "easyspec_prefill": ([ctxp, i32p, C.c_int, C.c_int], C.c_int),
             "calibrate_kv": ([ctxp, C.c_int, C.c_float, C.c_uint64], C.c_int),
+            "es_set_calibration": ([ctxp, C.c_int], C.c_int),
             "draft_step": ([ctxp, C.c_int, C.c_int, C.c_float, C.c_uint64, i32p], C.c_int),
             "verify_step": ([ctxp, C.c_float, C.c_uint64, i32p, i32p], C.c_int),
             "generate": ([ctxp, i32p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_float, C.c_uint64, i32p, C.POINTER(es_stats)], C.c_int),
@@ -186,6 +187,11 @@ class EasySpec:
 
     def calibrate_kv(self, gamma: int, temperature: float, seed: int):
         self._check(self._lib.calibrate_kv(self.ctx, gamma, temperature, seed))
+
+    def es_set_calibration(self, on: bool):
+        """on=False: the calibration ablation (accepted drafts keep their
+        layer-parallel KV entries)."""
+        self._check(self._lib.es_set_calibration(self.ctx, 1 if on else 0))
 
     def draft_step(self, k: int, gamma: int, temperature: float, seed: int):
         import numpy as np

@@ -34,9 +34,9 @@ class Pair:
         return EasySpec(self.wd, self.sd, self.wb, self.sb, self.dtype, max_batch, max_seq,
                         max_gamma, mode, None if groups is None else starts_of(groups))
 
-    def oracle(self, k=1, mode=ES_FULL_LAYER, groups=None, max_len=256):
+    def oracle(self, k=1, mode=ES_FULL_LAYER, groups=None, max_len=256, calibrate=True):
         return spec.SpecDecoder(self.Wd, self.shape_d, self.Wb, self.shape_b, groups=groups,
-                                k=k, mode=MODES[mode], max_len=max_len)
+                                k=k, mode=MODES[mode], max_len=max_len, calibrate=calibrate)
 
 
 def rel_l2(a, b):
