@@ -62,6 +62,8 @@ def parse():
                     help="sequences decoded together (the batched long-context workload: 1, 4 or 16)")
     ap.add_argument("--sigma", type=float, default=None,
                     help="self-draft workloads: draft = base + N(0, (sigma*0.02)^2)")
+    ap.add_argument("--layout", default=None,
+                    help="named draft layer-set layout (layouts.candidates); replaces --k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -236,8 +238,13 @@ def run_ours(args, rank: int, world: int):
     stream = torch.cuda.Stream()
     mode = ES_FULL_LAYER if args.mode == "full" else ES_ATTN_ONLY
     max_seq = ((P + max_new + 2 * gamma + 2) + 63) // 64 * 64
+    gs = None
+    if args.layout:
+        from layer_drafting_draft_b300 import layouts
+        sets = layouts.candidates(wl["draft"]["n_layers"])[args.layout]
+        gs, k = layouts.starts(sets), 0
     g = EasySpec(draft_w, wl["draft"], base_w, wl["base"], wl["dtype"], B, max_seq, gamma, mode,
-                 None, stream)
+                 gs, stream)
     seed0 = 1000 * rank
 
     def one_decode(step):
@@ -325,6 +332,7 @@ def run_ours(args, rank: int, world: int):
         "scaling": "weak", "vs_baseline": None, "dtype": wl["dtype"], "data": "synthetic",
         "config": {"workload": args.workload, "draft": shape_str(wl["draft"]), "base": shape_str(wl["base"]),
                    "batch": B, "prompt": P, "max_new": max_new, "gamma": gamma, "k": k, "mode": args.mode,
+                   **({"layout": args.layout} if args.layout else {}),
                    "temperature": T, "sigma": args.sigma, "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2 (weights {(pb['draft'] + pb['verify']) / 1e9:.1f} GB "
                          f"streamed per phase)"},
