@@ -101,10 +101,11 @@ def phase_bytes(wl: dict, gamma: int, ctx: int, B: int = 1) -> dict:
     return {"draft_fwd": draft_fwd, "draft": draft, "fuzzy": fuzzy, "verify": verify}
 
 
-def measured_traffic(kernel: str):
+def measured_traffic(kernel: str, workload: str, rows: int):
     """DRAM bytes per launch of `kernel` from the committed ncu summary
-    (profiles/traffic.json), or None when there is none or the kernel source
-    has changed since the counters were taken (sha256 of its files)."""
+    (profiles/traffic.json), or None when there is none for this workload and
+    number of activation rows, or the kernel source has changed since the
+    counters were taken (sha256 of its files)."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
@@ -112,7 +113,7 @@ def measured_traffic(kernel: str):
     with open(path) as f:
         t = json.load(f)
     e = t.get(kernel)
-    if not e:
+    if not e or e.get("workload") != workload or e.get("rows") != rows:
         return None
     h = hashlib.sha256()
     for rel in e["sources"]:
@@ -354,7 +355,7 @@ def run_ours(args, rank: int, world: int):
         "acceptance": {"tokens_per_phase": round(tok_per_phase, 3),
                        "rate": round(accepted / max(drafted, 1), 4)},
         "roofline": {"bound": "hbm", "kernel": name, "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": measured_traffic(name),
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": measured_traffic(name, args.workload, B * (gamma + 1)),
                      "launches": pn, "share_of_device_time": round(pms / total_prof_ms, 4),
                      "peak_source": peak_src},
         "clocks": clk, "gpu_launches": int(launches),

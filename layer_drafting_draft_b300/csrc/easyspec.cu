@@ -101,8 +101,9 @@ struct es_ctx {
     cublasHandle_t blas = nullptr;
     void* blas_ws = nullptr;
     size_t blas_ws_bytes = 0;
-    bf16 *tc_hi = nullptr, *tc_lo = nullptr;
-    float *tc_g = nullptr, *tc_u = nullptr;
+    bf16* tc_x = nullptr;                     // stacked planes [hi; lo] of one source, [2M][K]
+    float *tc_g = nullptr, *tc_u = nullptr;   // [2M][Nc] products (gate / up, or the op's)
+    size_t tc_cap = 0;                        // floats in tc_g and in tc_u
     cudaStream_t st = nullptr;
     bool own_stream = false;
     int dev = 0, num_sms = 148;
@@ -734,35 +735,43 @@ void gemm_many_rows(es_ctx* c, const Rec& r) {
         CK(cudaEventRecord(ev0, c->st));
     }
     blas_check(cublasSetStream(c->blas, c->st), __LINE__);
+    // Both planes of a source go through one GEMM as 2M activation rows, so
+    // every weight row is streamed once; the epilogue adds the two halves.
+    // Ops of one pass do not read each other's outputs, so a source split for
+    // one op serves the next ones too.
+    int split_xs = -1;
+    const float one = 1.0f, zero = 0.0f;
     for (int oi = 0; oi < L.nops; ++oi) {
         const GvOp& o = L.ops[oi];
         const bool swi = o.epi == GEPI_SWIGLU;
-        float* tgt[2] = {swi ? c->tc_g : o.y, c->tc_u};
-        const int ldt[2] = {swi ? o.N : o.ldy, o.N};
-        bool first[2] = {o.epi == GEPI_STORE || swi, true};  // beta = 0 for the first product
-        for (int si = 0; si < o.nseg; ++si) {
-            const GvSeg& sg = L.segs[o.seg0 + si];
-            const GvXSrc& x = L.xs[sg.xs];
-            if (x.K != sg.K || sg.K % 4) arg_fail(ES_ERR_ARG, "internal: many-row segment width %d", sg.K);
-            const int items = M * (sg.K / 4);
-            launch(c, "split_hilo", 0.0, split_hilo_kernel, dim3(std::min(4 * c->num_sms, (items + 255) / 256)),
-                   dim3(256), (size_t)0, x.src, x.ld, x.row_stride, x.row_off, M, sg.K, c->tc_hi, c->tc_lo);
-            const int set = sg.set;
-            const float one = 1.0f, zero = 0.0f;
-            for (int plane = 0; plane < 2; ++plane) {
-                const float* beta = first[set] ? &zero : &one;
-                blas_check(cublasGemmEx(c->blas, CUBLAS_OP_T, CUBLAS_OP_N, o.N, M, sg.K, &one, sg.W, CUDA_R_16BF,
-                                        sg.K, plane ? c->tc_lo : c->tc_hi, CUDA_R_16BF, sg.K, beta, tgt[set],
-                                        CUDA_R_32F, ldt[set], CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT),
+        float* scr[2] = {c->tc_g, c->tc_u};
+        const int cw = (int)std::min<size_t>((size_t)o.N, c->tc_cap / (2 * (size_t)M));  // columns per chunk
+        for (int n0 = 0; n0 < o.N; n0 += cw) {
+            const int nc = std::min(cw, o.N - n0);
+            bool first[2] = {true, true};
+            for (int si = 0; si < o.nseg; ++si) {
+                const GvSeg& sg = L.segs[o.seg0 + si];
+                const GvXSrc& x = L.xs[sg.xs];
+                if (x.K != sg.K || sg.K % 4) arg_fail(ES_ERR_ARG, "internal: many-row segment width %d", sg.K);
+                if (sg.xs != split_xs) {
+                    const int items = M * (sg.K / 4);
+                    launch(c, "split_hilo", 0.0, split_hilo_kernel,
+                           dim3(std::min(4 * c->num_sms, (items + 255) / 256)), dim3(256), (size_t)0, x.src, x.ld,
+                           x.row_stride, x.row_off, M, sg.K, c->tc_x, c->tc_x + (size_t)M * sg.K);
+                    split_xs = sg.xs;
+                }
+                const int set = sg.set;
+                blas_check(cublasGemmEx(c->blas, CUBLAS_OP_T, CUBLAS_OP_N, nc, 2 * M, sg.K, &one,
+                                        (const bf16*)sg.W + (size_t)n0 * sg.K, CUDA_R_16BF, sg.K, c->tc_x,
+                                        CUDA_R_16BF, sg.K, first[set] ? &zero : &one, scr[set], CUDA_R_32F, nc,
+                                        CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT),
                            __LINE__);
                 first[set] = false;
             }
-        }
-        if (swi || o.epi == GEPI_ACC_ADD) {
-            const int n = M * o.N;
-            launch(c, "epi_rows", 0.0, epi_rows_kernel, dim3(std::min(4 * c->num_sms, (n + 255) / 256)), dim3(256),
-                   (size_t)0, o.y, o.ldy, swi ? nullptr : o.add, swi ? c->tc_g : nullptr,
-                   swi ? c->tc_u : nullptr, M, o.N);
+            const size_t n = (size_t)M * nc;
+            launch(c, "epi_hilo", 0.0, epi_hilo_kernel, dim3((unsigned)std::min<size_t>(4 * c->num_sms, (n + 255) / 256)),
+                   dim3(256), (size_t)0, o.y + n0, o.ldy, o.epi == GEPI_ACC_ADD ? o.add + n0 : nullptr, (int)o.epi,
+                   (const float*)c->tc_g, swi ? (const float*)c->tc_u : nullptr, M, nc);
         }
     }
     if (c->profiling) {
@@ -1300,17 +1309,17 @@ es_status easyspec_init(const es_config* cfg, const es_weights* draft, const es_
             for (const Model* mm : {&c->md, &c->mb}) {
                 rows = std::max(rows, (size_t)mm->Mw);
                 kmax = std::max({kmax, (size_t)mm->d, (size_t)mm->qd, (size_t)mm->F});
-                fmax = std::max(fmax, (size_t)mm->F);
+                fmax = std::max({fmax, (size_t)mm->F, (size_t)mm->d, (size_t)mm->qd});
             }
             if (cublasCreate(&c->blas) != CUBLAS_STATUS_SUCCESS) arg_fail(ES_ERR_CUDA, "cublasCreate failed");
             c->blas_ws_bytes = (size_t)32 << 20;
             c->blas_ws = c->dalloc<char>(c->blas_ws_bytes);
             blas_check(cublasSetWorkspace(c->blas, c->blas_ws, c->blas_ws_bytes), __LINE__);
             blas_check(cublasSetStream(c->blas, c->st), __LINE__);
-            c->tc_hi = c->dalloc<bf16>(rows * kmax);
-            c->tc_lo = c->dalloc<bf16>(rows * kmax);
-            c->tc_g = c->dalloc<float>(rows * fmax);
-            c->tc_u = c->dalloc<float>(rows * fmax);
+            c->tc_x = c->dalloc<bf16>(2 * rows * kmax);
+            c->tc_cap = 2 * rows * fmax;
+            c->tc_g = c->dalloc<float>(c->tc_cap);
+            c->tc_u = c->dalloc<float>(c->tc_cap);
         }
         c->gv_counters = c->dalloc<int>(GV_COUNTERS);
         c->gv_done = c->dalloc<int>(1);

@@ -132,18 +132,29 @@ __global__ void split_hilo_kernel(const float* __restrict__ src, int ld, int rs,
 
 // Epilogues of a many-row weight pass after its GEMMs: y += add
 // (residual + delta) or y = silu(g) * u (SwiGLU); y [M][ldy], g/u [M][N].
-__global__ void epi_rows_kernel(float* __restrict__ y, int ldy, const float* __restrict__ add,
-                                const float* __restrict__ g, const float* __restrict__ u, int M, int N) {
+// Epilogue of a many-row pass over output columns [0, Nc) of y (already
+// offset to the chunk): the GEMM of the stacked planes [hi; lo] left the hi
+// products in rows 0..M-1 of s and the lo products in rows M..2M-1 ([2M][Nc]),
+// so row m of the result is s[m] + s[M + m] (s1 likewise for the up
+// projection of a SwiGLU op).
+__global__ void epi_hilo_kernel(float* __restrict__ y, int ldy, const float* __restrict__ add, int epi,
+                                const float* __restrict__ s0, const float* __restrict__ s1, int M, int Nc) {
     grid_dep_wait();
     grid_dep_launch();
-    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < M * N; t += gridDim.x * blockDim.x) {
-        const int m = t / N, n = t - m * N;
+    const size_t half = (size_t)M * Nc;
+    for (size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x; t < half; t += (size_t)gridDim.x * blockDim.x) {
+        const int m = (int)(t / Nc), n = (int)(t - (size_t)m * Nc);
         float* yp = y + (size_t)m * ldy + n;
-        if (g) {
-            const float a = g[t];
-            *yp = a / (1.0f + expf(-a)) * u[t];
-        } else {
-            *yp += add[(size_t)m * ldy + n];
+        const float a = s0[t] + s0[half + t];
+        switch (epi) {
+            case GEPI_SWIGLU: {
+                const float b = s1[t] + s1[half + t];
+                *yp = a / (1.0f + expf(-a)) * b;
+                break;
+            }
+            case GEPI_STORE: *yp = a; break;
+            case GEPI_ACC: *yp = *yp + a; break;
+            default: *yp = *yp + a + add[(size_t)m * ldy + n]; break;
         }
     }
 }
