@@ -260,6 +260,15 @@ ES_API es_status es_read_dist(es_ctx *ctx, int which, float *out);
 ES_API es_status es_read_tokens(es_ctx *ctx, int seq, int32_t *out, int cap,
                          int *n_committed);
 
+/* The draft layer sets that set size k gives when no explicit sets are
+ * configured ([DISC] reply on Table 4 / Appendix B.1): layer 0 and layer
+ * n_layers-1 alone, the layers between in blocks aligned to multiples of k;
+ * k = 1 gives one set per layer.  Writes the first layer of each set to
+ * starts[0..min(cap, *n_sets)) (host int32, caller-owned) and the number of
+ * sets to *n_sets (cap 0 and starts NULL query the count).  Host only: needs
+ * no context and no GPU.  ES_ERR_ARG unless n_layers >= 1 and 1 <= k <= 8. */
+ES_API es_status es_layer_sets(int n_layers, int k, int32_t *starts, int cap, int *n_sets);
+
 ES_API const char *easyspec_last_error(const es_ctx *ctx);
 ES_API void easyspec_destroy(es_ctx *ctx);
 

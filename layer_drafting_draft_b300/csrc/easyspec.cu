@@ -1642,6 +1642,14 @@ es_status es_read_tokens(es_ctx* c, int seq, int32_t* out, int cap, int* n_commi
     });
 }
 
+es_status es_layer_sets(int n_layers, int k, int32_t* starts, int cap, int* n_sets) {
+    if (n_layers < 1 || k < 1 || k > MAX_GROUP || !n_sets || cap < 0 || (cap > 0 && !starts)) return ES_ERR_ARG;
+    const auto sets = default_sets(n_layers, k);
+    *n_sets = (int)sets.size();
+    for (int i = 0; i < (int)sets.size() && i < cap; ++i) starts[i] = sets[i].front();
+    return ES_OK;
+}
+
 const char* easyspec_last_error(const es_ctx* c) { return c ? c->err.c_str() : "null context"; }
 
 void easyspec_destroy(es_ctx* c) {

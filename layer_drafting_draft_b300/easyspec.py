@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "ES_OK", -1: "ES_ERR_ARG", -2: "ES_ERR_OOM", -3: "ES_ERR_CUDA
 EXPORTED = ["easyspec_init", "easyspec_prefill", "calibrate_kv", "es_set_calibration", "draft_step", "verify_step",
             "generate", "es_decode", "es_profile", "es_profile_read", "es_accept_resample",
             "es_accept_resample_noalloc",
-            "es_sample", "es_read_kv", "es_read_dist", "es_read_tokens", "easyspec_last_error",
+            "es_sample", "es_read_kv", "es_read_dist", "es_read_tokens", "es_layer_sets", "easyspec_last_error",
             "easyspec_destroy"]
 
 
@@ -89,6 +89,7 @@ def lib() -> C.CDLL:
             "es_read_kv": ([ctxp, C.c_int, C.c_int, C.c_int, C.c_int, f32p, f32p], C.c_int),
             "es_read_dist": ([ctxp, C.c_int, f32p], C.c_int),
             "es_read_tokens": ([ctxp, C.c_int, i32p, C.c_int, C.POINTER(C.c_int)], C.c_int),
+            "es_layer_sets": ([C.c_int, C.c_int, i32p, C.c_int, C.POINTER(C.c_int)], C.c_int),
             "easyspec_last_error": ([ctxp], C.c_char_p),
             "easyspec_destroy": ([ctxp], None),
         }
@@ -98,6 +99,19 @@ def lib() -> C.CDLL:
             f.restype = res
         _lib = L
     return _lib
+
+
+def layer_sets(n_layers: int, k: int) -> list[int]:
+    """The library's default draft layer sets for set size k, as the first
+    layer of each set (host only, no GPU)."""
+    import numpy as np
+    L = lib()
+    n = C.c_int(0)
+    out = np.zeros(max(n_layers, 1), dtype=np.int32)
+    st = L.es_layer_sets(n_layers, k, out.ctypes.data_as(C.POINTER(C.c_int32)), len(out), C.byref(n))
+    if st != ES_OK:
+        raise EasySpecError(st, "es_layer_sets: invalid arguments")
+    return out[: n.value].tolist()
 
 
 class EasySpecError(RuntimeError):

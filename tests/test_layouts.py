@@ -70,3 +70,26 @@ def test_search_ranks_by_decode_rate():
     assert rows[-1]["layout"] == "sequential"
     r = rows[0]
     assert r["tok_s"] == pytest.approx(240 / (r["ms_per_phase"] * 100 / 1e3))
+
+
+# ------------------------------------------------ the library's own rule
+# es_layer_sets returns the set starts the CUDA path's planner uses when no
+# explicit sets are configured (host only, no GPU).
+
+def test_library_rule_matches_the_pages_example():
+    from layer_drafting_draft_b300.easyspec import layer_sets
+    assert layer_sets(32, 4) == LY.starts(_golden())
+
+
+@pytest.mark.parametrize("L", [1, 2, 3, 5, 8, 16, 24, 28, 32, 80])
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8])
+def test_library_rule_agrees_with_the_oracle(L, N):
+    from layer_drafting_draft_b300.easyspec import layer_sets
+    assert layer_sets(L, N) == LY.starts(M.default_groups(L, N))
+
+
+def test_library_rule_rejects_bad_arguments():
+    from layer_drafting_draft_b300.easyspec import EasySpecError, layer_sets
+    for L, N in ((0, 4), (8, 0), (8, 9)):
+        with pytest.raises(EasySpecError):
+            layer_sets(L, N)
