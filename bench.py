@@ -242,7 +242,10 @@ def run_ours(args, rank: int, world: int):
     gs = None
     if args.layout:
         from layer_drafting_draft_b300 import layouts
-        sets = layouts.candidates(wl["draft"]["n_layers"])[args.layout]
+        cands = layouts.candidates(wl["draft"]["n_layers"])
+        if args.layout not in cands:
+            raise SystemExit(f"--layout {args.layout}: not one of {', '.join(cands)}")
+        sets = cands[args.layout]
         gs, k = layouts.starts(sets), 0
     g = EasySpec(draft_w, wl["draft"], base_w, wl["base"], wl["dtype"], B, max_seq, gamma, mode,
                  gs, stream)

@@ -205,6 +205,9 @@ def main(argv=None):
     ps = synth.make_prompts(a.prompts, prompts.shape[1], wl["draft"]["vocab"], 91).numpy()
     cands = candidates(wl["draft"]["n_layers"])
     if a.layouts:
+        bad = [k for k in a.layouts.split(",") if k not in cands]
+        if bad:
+            raise SystemExit(f"--layouts: unknown {', '.join(bad)}; known: {', '.join(cands)}")
         cands = {k: cands[k] for k in a.layouts.split(",")}
     mode = ES_FULL_LAYER if a.mode == "full" else ES_ATTN_ONLY
     rows = search(gpu_measure(wl, wd, wb, ps, mode, gamma, a.max_new, a.temperature), cands)
