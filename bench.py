@@ -172,7 +172,7 @@ class Clocks:
 
 
 # ------------------------------------------------------------------ CPU oracle
-def oracle_sample(wl: dict, gamma: int, tokens_per_phase: float, reps: int = 2, seed: int = 0):
+def oracle_sample(wl: dict, gamma: int, tokens_per_phase: float, reps: int = 24, seed: int = 0):
     """Time the CPU oracle on a bounded sample of the workload: one exact
     decoder layer and the output head of each model at full width (2-layer
     truncated models, float64 numpy, context ~prompt+64 filled with random
@@ -190,7 +190,7 @@ def oracle_sample(wl: dict, gamma: int, tokens_per_phase: float, reps: int = 2, 
         s = dict(wl[which], n_layers=2)
         W = M.as_f64_weights(synth.make_weights(s, 7 + seed, wl["dtype"], dev))
         shape = M.Shape(**s)
-        cache = M.KVCache(shape, ctx + 8)
+        cache = M.KVCache(shape, ctx + reps + 8)
         r = np.random.default_rng(1)
         cache.K[:, :ctx] = r.normal(size=cache.K[:, :ctx].shape)
         cache.V[:, :ctx] = r.normal(size=cache.V[:, :ctx].shape)
