@@ -364,7 +364,8 @@ def run_ours(args, rank: int, world: int):
         "clocks": clk, "gpu_launches": int(launches),
         "timed_wall_s": round(wall, 3),
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    # the CPU oracle's figure belongs to the single-GPU line only
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(wl, gamma, tok_per_phase)
     if rank == 0:
         print(json.dumps(line), flush=True)
