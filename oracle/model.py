@@ -46,11 +46,16 @@ N=4 example "0, 1~4, 4~7, ..., 28~30" with 28, 29, 30 forming a 3-set because
 31 is the last layer): layer 0 and layer L-1 are singletons; layers 1..L-2 are
 cut into the aligned blocks [mN, mN+N-1], the first and last blocks clipped.
 
+``forward_block`` is the exact forward of a run of consecutive tokens in one
+go (matrix products over the run), for long prompts; it computes what
+``forward_exact`` computes token by token.
+
 Parity: pinned by tests/test_oracle_model.py (closed forms for zeroed weights,
 RoPE identity at position 0 and relative-position invariance, single-position
 attention, an independent full-sequence causal forward, cosine invariance of
 gain-free RMSNorm (reply on Table 3), set size 1 == sequential, brute-force
-delta sums for FULL_LAYER, the grouping example).
+delta sums for FULL_LAYER, the grouping example, the block forward equal to
+the token-by-token one).
 """
 from __future__ import annotations
 
@@ -254,3 +259,73 @@ def forward_fuzzy(W, shape: Shape, token: int, pos: int, cache: KVCache,
         hidden.append(h)
     z = head_logits(W, shape, h)
     return (z, hidden) if return_hidden else z
+
+
+# ------------------------------------------------------- block forward (long prompts)
+
+def rms_norm_rows(X, g, eps):
+    """rms_norm applied to every row of X [T, d]."""
+    return X / np.sqrt(np.mean(X * X, axis=-1, keepdims=True) + eps) * g
+
+
+def rope_rows(x, pos, theta: float):
+    """rope() of every row: x [T, n, hd], row t rotated to position pos[t]."""
+    hd = x.shape[-1]
+    half = hd // 2
+    i = np.arange(half, dtype=np.float64)
+    ang = np.asarray(pos, dtype=np.float64)[:, None] * theta ** (-2.0 * i / hd)
+    c, s = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+    a, b = x[..., :half], x[..., half:]
+    return np.concatenate([a * c - b * s, b * c + a * s], axis=-1)
+
+
+def attend_rows(q, K, V, pos, n_heads: int, n_kv: int):
+    """attend() for several query rows at once.
+
+    q : [T, H, hd] (row t at position pos[t]); K, V : [P, Hkv, hd] with P >
+    max(pos).  Row t sees positions 0..pos[t] (causal).  Returns [T, H*hd].
+    """
+    T, _, hd = q.shape
+    group = n_heads // n_kv
+    visible = np.arange(K.shape[0])[None, :] <= np.asarray(pos)[:, None]
+    out = np.empty((T, n_heads, hd))
+    for h in range(n_heads):
+        kvh = h // group
+        s = q[:, h, :] @ K[:, kvh, :].T / np.sqrt(hd)
+        s = np.where(visible, s, -np.inf)
+        s = np.exp(s - s.max(axis=-1, keepdims=True))
+        out[:, h] = (s / s.sum(axis=-1, keepdims=True)) @ V[:, kvh, :]
+    return out.reshape(T, -1)
+
+
+def forward_block(W, shape: Shape, tokens, pos0: int, cache: KVCache, logit_rows=None):
+    """Exact forward of consecutive tokens, token t at position pos0 + t.
+
+    The result is that of calling forward_exact on each token in order (the
+    same exact model, written with matrix products over the block): every
+    row writes its K/V at its position and attends to positions 0..its own,
+    which for rows of the block include the block's earlier rows.  Returns
+    the float64 logits of the rows listed in ``logit_rows`` (all rows when
+    None), [len(rows), V].
+    """
+    T = len(tokens)
+    pos = pos0 + np.arange(T)
+    hd = shape.head_dim
+    H = W["embed"][np.asarray(tokens, dtype=np.int64)].astype(np.float64)
+    for l in range(shape.n_layers):
+        lw = W["layers"][l]
+        X = rms_norm_rows(H, lw["attn_norm"], shape.eps)
+        q = rope_rows((X @ lw["wq"].T).reshape(T, shape.n_heads, hd), pos, shape.rope_theta)
+        k = rope_rows((X @ lw["wk"].T).reshape(T, shape.n_kv_heads, hd), pos, shape.rope_theta)
+        v = (X @ lw["wv"].T).reshape(T, shape.n_kv_heads, hd)
+        cache.K[l, pos0:pos0 + T] = k
+        cache.V[l, pos0:pos0 + T] = v
+        a = attend_rows(q, cache.K[l, :pos0 + T], cache.V[l, :pos0 + T], pos,
+                        shape.n_heads, shape.n_kv_heads)
+        H = H + a @ lw["wo"].T
+        Y = rms_norm_rows(H, lw["mlp_norm"], shape.eps)
+        H = H + (silu(Y @ lw["wgate"].T) * (Y @ lw["wup"].T)) @ lw["wdown"].T
+    rows = np.arange(T) if logit_rows is None else np.asarray(logit_rows, dtype=np.int64)
+    if len(rows) == 0:
+        return np.zeros((0, shape.vocab))
+    return rms_norm_rows(H[rows], W["final_norm"], shape.eps) @ W["lm_head"].T

@@ -76,7 +76,7 @@ class SpecDecoder:
 
     def __init__(self, Wd, shape_d: M.Shape, Wb, shape_b: M.Shape,
                  groups=None, k: int = 1, mode: int = M.FULL_LAYER,
-                 max_len: int = 256, calibrate: bool = True):
+                 max_len: int = 256, calibrate: bool = True, block: bool = False):
         if shape_d.vocab != shape_b.vocab:
             raise ValueError("draft and base must share one vocabulary")
         self.Wd, self.sd, self.Wb, self.sb = Wd, shape_d, Wb, shape_b
@@ -85,6 +85,10 @@ class SpecDecoder:
         self.mode = mode
         self.max_len = max_len
         self.calibrate = calibrate
+        # exact multi-token forwards (prompt prefill, calibration, verify) run
+        # as one block forward instead of token by token: the same model,
+        # fast enough for prompts of thousands of tokens
+        self.block = block
         self.rows: list[Row] = []
 
     # -------------------------------------------------------------- stages
@@ -93,15 +97,22 @@ class SpecDecoder:
         for prompt in prompts:
             r = Row(self.sd, self.sb, self.max_len)
             r.tokens = [int(t) for t in prompt]
-            for pos in range(len(r.tokens) - 1):
-                M.forward_exact(self.Wb, self.sb, r.tokens[pos], pos, r.base)
+            if self.block:
+                M.forward_block(self.Wb, self.sb, r.tokens[:-1], 0, r.base, logit_rows=[])
+            else:
+                for pos in range(len(r.tokens) - 1):
+                    M.forward_exact(self.Wb, self.sb, r.tokens[pos], pos, r.base)
             self.rows.append(r)
 
     def calibrate_row(self, r: Row):
         """Exact draft forward over pending tokens; returns last row's logits."""
         z = None
-        for pos in range(r.draft_len, len(r.tokens)):
-            z = M.forward_exact(self.Wd, self.sd, r.tokens[pos], pos, r.draft)
+        if self.block and len(r.tokens) - r.draft_len > 1:
+            z = M.forward_block(self.Wd, self.sd, r.tokens[r.draft_len:], r.draft_len, r.draft,
+                                logit_rows=[len(r.tokens) - r.draft_len - 1])[0]
+        else:
+            for pos in range(r.draft_len, len(r.tokens)):
+                z = M.forward_exact(self.Wd, self.sd, r.tokens[pos], pos, r.draft)
         r.draft_len = len(r.tokens)
         return z
 
@@ -135,10 +146,12 @@ class SpecDecoder:
         draws = None if greedy else phase_draws(seed, b, r.phase, gamma)
         n = len(r.tokens)
         zp, p = [], []
-        for j, tok in enumerate([r.tokens[-1]] + list(r.d)):
-            z = M.forward_exact(self.Wb, self.sb, tok, n - 1 + j, r.base)
-            zp.append(z)
-            p.append(_dist(z, temperature))
+        run = [r.tokens[-1]] + list(r.d)
+        if self.block:
+            zp = list(M.forward_block(self.Wb, self.sb, run, n - 1, r.base))
+        else:
+            zp = [M.forward_exact(self.Wb, self.sb, tok, n - 1 + j, r.base) for j, tok in enumerate(run)]
+        p = [_dist(z, temperature) for z in zp]
         r.zp, r.p = np.array(zp), np.array(p)
         a, new = accept_resample(r.p, r.q, r.d,
                                  None if greedy else draws[gamma:2 * gamma],

@@ -148,6 +148,31 @@ def test_incremental_forward_matches_full_sequence_textbook(which):
     assert np.max(np.abs(inc - ref)) < 1e-11 * max(1.0, np.max(np.abs(ref)))
 
 
+@pytest.mark.parametrize("which", ["draft", "base"])
+def test_block_forward_matches_textbook_and_token_by_token(which):
+    """The block forward over a whole sequence equals the independent
+    textbook forward; a block that starts after a token-by-token prefix
+    leaves the same cache and logits as continuing token by token."""
+    Wd, sd, Wb, sb = tiny_pair(3, std=0.2)
+    W, s = (Wd, sd) if which == "draft" else (Wb, sb)
+    toks = [3, 17, 17, 40, 2, 63, 0, 11, 9, 9, 30]
+    ref = _textbook_logits(W, s, toks)
+    cb = M.KVCache(s, 16)
+    blk = M.forward_block(W, s, toks, 0, cb)
+    assert np.max(np.abs(blk - ref)) < 1e-11 * max(1.0, np.max(np.abs(ref)))
+    # prefix of 4 tokens one at a time, then the remaining 7 as one block
+    ci, cm = M.KVCache(s, 16), M.KVCache(s, 16)
+    inc = [M.forward_exact(W, s, t, p, ci) for p, t in enumerate(toks)]
+    for p, t in enumerate(toks[:4]):
+        M.forward_exact(W, s, t, p, cm)
+    tail = M.forward_block(W, s, toks[4:], 4, cm, logit_rows=[0, 6])
+    assert np.max(np.abs(tail - np.array([inc[4], inc[10]]))) < 1e-11 * max(1.0, np.max(np.abs(ref)))
+    n = len(toks)
+    assert np.max(np.abs(cm.K[:, :n] - ci.K[:, :n])) < 1e-12
+    assert np.max(np.abs(cm.V[:, :n] - ci.V[:, :n])) < 1e-12
+    assert np.max(np.abs(cb.K[:, :n] - ci.K[:, :n])) < 1e-12
+
+
 def _prefill(W, s, toks, cache):
     for p, t in enumerate(toks):
         M.forward_exact(W, s, t, p, cache)

@@ -227,3 +227,32 @@ def test_no_calibration_cache_keeps_accepted_fuzzy_entries(mode):
         M.forward_exact(Wd, sb, t, pos, exact)
     p = min(fuzzy_pos)
     assert not np.allclose(r.draft.K[:, p], exact.K[:, p])
+
+
+@pytest.mark.parametrize("temp", [0.0, 1.0])
+def test_block_forwards_leave_the_loop_unchanged(temp):
+    """The loop with its exact multi-token forwards run as block forwards
+    (prefill, calibration, verify) emits the same tokens and the same logits
+    to rounding as the token-by-token loop, and its calibrated draft cache
+    still equals a fresh sequential prefill."""
+    Wd, sd, Wb, sb = tiny_pair(12, std=0.3, Ld=5)
+    prompts = [[5, 6, 7, 8, 9, 10, 11], [60, 1, 2]]
+    a = spec.SpecDecoder(Wd, sd, Wb, sb, k=2, mode=M.FULL_LAYER, max_len=64)
+    b = spec.SpecDecoder(Wd, sd, Wb, sb, k=2, mode=M.FULL_LAYER, max_len=64, block=True)
+    a.prefill(prompts)
+    b.prefill(prompts)
+    for ph in range(5):
+        for r in range(2):
+            da = a.draft_row(r, 4, temp, 3)
+            db = b.draft_row(r, 4, temp, 3)
+            assert da == db
+            assert np.max(np.abs(a.rows[r].zq - b.rows[r].zq)) < 1e-10
+            assert a.verify_row(r, 4, temp, 3) == b.verify_row(r, 4, temp, 3)
+            assert np.max(np.abs(a.rows[r].zp - b.rows[r].zp)) < 1e-10
+    r = b.rows[0]
+    b.calibrate_row(r)
+    fresh = M.KVCache(sd, 64)
+    for pos, t in enumerate(r.tokens):
+        M.forward_exact(Wd, sd, t, pos, fresh)
+    n = len(r.tokens)
+    assert np.max(np.abs(r.draft.K[:, :n] - fresh.K[:, :n])) < 1e-11
