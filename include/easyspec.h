@@ -172,8 +172,10 @@ ES_API es_status draft_step(es_ctx *ctx, int k, int gamma, float temperature,
 ES_API es_status verify_step(es_ctx *ctx, float temperature, uint64_t seed,
                       int32_t *n_accepted, int32_t *tokens_out);
 
-/* Whole speculative generation: prefill, then phases of draft_step +
- * verify_step until every sequence has max_new new tokens (a sequence that
+/* Whole speculative generation ([ABS]: draft with layer-parallel sets, verify
+ * the drafts in one base forward, calibrate the draft KV; [DISC] Figure 2
+ * reply: fuzzy entries live for one phase and are then replaced): prefill,
+ * then phases of draft_step + verify_step until every sequence has max_new new tokens (a sequence that
  * has them stops committing while the others finish).  out: host int32
  * [B, max_new].  Needs P + max_new + 2*gamma + 2 <= max_seq
  * (ES_ERR_CAPACITY). */
@@ -181,7 +183,8 @@ ES_API es_status generate(es_ctx *ctx, const int32_t *prompts, int B, int P,
                    int max_new, int gamma, int k, float temperature,
                    uint64_t seed, int32_t *out, es_stats *stats);
 
-/* Decode max_new more tokens for every loaded sequence (after
+/* The decoding loop of generate() ([ABS]; [DISC] Figure 2 reply) without
+ * the prefill.  Decode max_new more tokens for every loaded sequence (after
  * easyspec_prefill or a previous decode): phases of draft_step + verify_step
  * as in generate(), with the tokens left on the device (read them with
  * es_read_tokens).  Needs n + max_new + 2*gamma + 2 <= max_seq for every
@@ -215,22 +218,26 @@ ES_API es_status es_accept_resample(const float *p, const float *q, const int32_
                              void *stream);
 
 /* es_accept_resample without any device allocation.  The pages have no
- * counterpart: this is for callers that cannot allocate device memory at the
- * point of the call -- code running while a CUDA stream is being captured
- * into a graph (cudaMalloc is not allowed there), latency-critical loops that
- * cannot take cudaMalloc's device-wide synchronisation, and hosts whose
- * device memory is owned by their own allocator.  es_accept_resample
- * allocates its scratch (per-chunk partials, masses, arrival counters) on
- * every call; this entry point uses a fixed array inside the library instead.
- *   Limits: B <= 16, gamma <= 16, and at most 160 vocabulary chunks (a chunk
- *   is max(512, ceil(V / SMs)) entries; 148 on a B300 for any V).  Larger
- *   sizes return ES_ERR_ARG (with a message on stderr).
- *   The array is shared by every call in the process on a device and keeps
- *   the last call's contents (the counters are cleared at each call): calls
- *   that overlap on the GPU -- on different streams, or from several host
- *   threads -- race and must not be issued.
- *   The first call on a device looks up the array's device address; make it
- *   before any stream capture that should contain later calls.
+ * counterpart.  es_accept_resample allocates its scratch (per-chunk partials,
+ * masses, arrival counters) with cudaMalloc on every call; some callers
+ * cannot do that where they call: a serving host that reserved the device's
+ * memory for its own pool allocator up front (cudaMalloc then fails, or
+ * takes memory the pool counts on), and a decode loop that cannot take
+ * cudaFree's device-wide synchronisation between tokens.  This entry point
+ * works in a fixed array inside the library instead.
+ *   Limits: B <= 16, gamma <= 16, and at most 160 vocabulary chunks.  A
+ *   chunk is max(512, ceil(V / SMs)) entries, so the call uses
+ *   min(SMs, ceil(V / 512)) chunks: any V fits on a device with at most 160
+ *   SMs (148 on a B300), and a device with more SMs refuses large V.
+ *   Larger sizes return ES_ERR_ARG (with a message on stderr).
+ *   The array (about 390 KB) is held by every GPU that loads the library
+ *   until the process exits.  It is shared by every call in the process on a
+ *   device and keeps the last call's contents (the arrival counters are
+ *   cleared at each call): calls that overlap on the GPU -- on different
+ *   streams, or from several host threads -- race and must not be issued.
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture
+ *   begins.
  * Arguments, layouts and results as es_accept_resample; synchronous on
  * `stream`. */
 ES_API es_status es_accept_resample_noalloc(const float *p, const float *q, const int32_t *d,

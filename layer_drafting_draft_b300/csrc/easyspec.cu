@@ -1203,9 +1203,12 @@ es_stats do_decode(es_ctx* c, int max_new, int gamma, int k, float temperature, 
 // ------------------------------------------------------------------ fixed scratch
 // Scratch of es_accept_resample_noalloc: a file-scope device array, so the
 // entry point never allocates.  Every GPU that loads the library holds it
-// until the process exits.  Layout: greedy argmax partials
-// [NOALLOC_MAX_B * 17 rows][NOALLOC_MAX_NB][2] floats, chunk masses
-// [NOALLOC_MAX_B][NOALLOC_MAX_NB][2] u64, arrival counters [NOALLOC_MAX_B].
+// until the process exits.  Three regions, each sized for the largest call
+// (B = NOALLOC_MAX_B, gamma = NOALLOC_MAX_GAMMA, NOALLOC_MAX_NB chunks): greedy
+// argmax partials (floats), chunk masses (u64) and arrival counters (int).  A
+// call packs its data densely from the start of each region with its own
+// row count and chunk count: partials [B*(gamma+1)][nb][2], masses [B][nb][2],
+// counters [B].
 constexpr int NOALLOC_MAX_B = 16;
 constexpr int NOALLOC_MAX_GAMMA = 16;
 constexpr int NOALLOC_MAX_NB = 160;

@@ -273,11 +273,35 @@ class EasySpec:
         return out[: n.value]
 
 
+def _check_accept_args(p, q, d, u, greedy: bool):
+    """The kernels read p, q, d and u as dense device arrays of the sizes that
+    p's shape implies: refuse anything else here rather than let a kernel
+    read past a buffer."""
+    if p.dim() != 3:
+        raise ValueError("p must be [B, gamma+1, V]")
+    B, g1, V = p.shape
+    want = [("p", p, torch.float32, (B, g1, V)), ("q", q, torch.float32, (B, g1 - 1, V)),
+            ("d", d, torch.int32, (B, g1 - 1))]
+    if u is not None or not greedy:
+        if u is None:
+            raise ValueError("sampled accept/resample needs the draws u")
+        want.append(("u", u, torch.int64, (B, g1)))
+    for name, t, dt, shp in want:
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dtype != dt or tuple(t.shape) != shp or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {dt} tensor of shape {shp}, "
+                             f"got {t.dtype} {tuple(t.shape)}")
+        if t.device != p.device:
+            raise ValueError(f"{name} is on {t.device}, p on {p.device}")
+    return B, g1, V
+
+
 def es_accept_resample(p: torch.Tensor, q: torch.Tensor, d: torch.Tensor, u: torch.Tensor | None,
                        greedy: bool):
     """Accept/resample on device tensors: p [B,g+1,V] f32, q [B,g,V] f32,
     d [B,g] int32, u [B,g+1] uint64 (as int64).  Returns (n_acc, tok)."""
-    B, g1, V = p.shape
+    B, g1, V = _check_accept_args(p, q, d, u, greedy)
     n_acc = torch.empty(B, dtype=torch.int32, device=p.device)
     tok = torch.empty(B, g1, dtype=torch.int32, device=p.device)
     st = lib().es_accept_resample(_ptr(p), _ptr(q), _ptr(d), _ptr(u) if u is not None else None,
@@ -293,7 +317,7 @@ def es_accept_resample_noalloc(p: torch.Tensor, q: torch.Tensor, d: torch.Tensor
     """es_accept_resample through the entry point that allocates no device
     memory (fixed scratch inside the library; B <= 16, gamma <= 16).
     Only the outputs are allocated here, by the caller's side."""
-    B, g1, V = p.shape
+    B, g1, V = _check_accept_args(p, q, d, u, greedy)
     n_acc = torch.empty(B, dtype=torch.int32, device=p.device)
     tok = torch.empty(B, g1, dtype=torch.int32, device=p.device)
     st = lib().es_accept_resample_noalloc(_ptr(p), _ptr(q), _ptr(d), _ptr(u) if u is not None else None,

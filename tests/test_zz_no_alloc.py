@@ -1,12 +1,13 @@
 """The accept/resample entry point that allocates no device memory.
 
 es_accept_resample_noalloc serves callers that cannot allocate device memory
-where they call it (inside a stream capture, in latency-critical loops, under
-a host-owned allocator).  It uses a fixed scratch array inside the library
-instead of allocating, so two things are checked here: its decisions equal
-those of es_accept_resample on the same inputs, and a second call right after
-the first (the array still holding the first call's contents) is as correct
-as the first.  Sizes beyond the array are refused.
+where they call it: a serving host whose device memory is reserved up front
+for its own pool allocator, or a decode loop that cannot take cudaFree's
+device-wide synchronisation between tokens.  It uses a fixed scratch array
+inside the library instead of allocating, so two things are checked here:
+its decisions equal those of es_accept_resample on the same inputs, and a
+second call right after the first (the array still holding the first call's
+contents) is as correct as the first.  Sizes beyond the array are refused.
 
 This file is collected last on purpose: if it fails, a run that stops at the
 first failure has already run every other test.
