@@ -137,12 +137,32 @@ def attend(q, K, V, n_heads: int, n_kv: int):
     return out.reshape(-1)
 
 
-class KVCache:
-    """Per-model cache: K, V of shape [L, max_len, Hkv, hd] (float64)."""
+def round_bf16(x):
+    """Values of x (float64) as stored in bfloat16: rounded to float32, then
+    to the nearest bfloat16 (8 significant bits), ties to even, returned as
+    float64.  A bfloat16 is the upper half of a float32's bit pattern."""
+    b = np.ascontiguousarray(np.asarray(x, dtype=np.float32)).view(np.uint32).astype(np.uint64)
+    keep = b >> 16
+    rest = b & 0xFFFF
+    up = (rest > 0x8000) | ((rest == 0x8000) & ((keep & 1) == 1))
+    keep = keep + up.astype(np.uint64)
+    return ((keep << 16).astype(np.uint32)).view(np.float32).astype(np.float64)
 
-    def __init__(self, shape: Shape, max_len: int):
+
+class KVCache:
+    """Per-model cache: K, V of shape [L, max_len, Hkv, hd] (float64).
+
+    ``dtype`` is the storage precision of the entries: "f64" keeps them as
+    computed; "bf16" stores round_bf16 of every entry (a bf16 model's cache),
+    and every later read, the writing position's own included, sees the
+    stored value."""
+
+    def __init__(self, shape: Shape, max_len: int, dtype: str = "f64"):
+        if dtype not in ("f64", "bf16"):
+            raise ValueError("cache dtype must be 'f64' or 'bf16'")
         self.K = np.zeros((shape.n_layers, max_len, shape.n_kv_heads, shape.head_dim))
         self.V = np.zeros_like(self.K)
+        self.store = round_bf16 if dtype == "bf16" else (lambda x: x)
 
 
 # ---------------------------------------------------------------- sublayers
@@ -155,8 +175,8 @@ def attn_delta(lw, shape: Shape, x_normed, pos: int, cache: KVCache, l: int):
     v = (lw["wv"] @ x_normed).reshape(shape.n_kv_heads, hd)
     q = rope(q, pos, shape.rope_theta)
     k = rope(k, pos, shape.rope_theta)
-    cache.K[l, pos] = k
-    cache.V[l, pos] = v
+    cache.K[l, pos] = cache.store(k)
+    cache.V[l, pos] = cache.store(v)
     a = attend(q, cache.K[l, : pos + 1], cache.V[l, : pos + 1],
                shape.n_heads, shape.n_kv_heads)
     return lw["wo"] @ a
@@ -318,8 +338,8 @@ def forward_block(W, shape: Shape, tokens, pos0: int, cache: KVCache, logit_rows
         q = rope_rows((X @ lw["wq"].T).reshape(T, shape.n_heads, hd), pos, shape.rope_theta)
         k = rope_rows((X @ lw["wk"].T).reshape(T, shape.n_kv_heads, hd), pos, shape.rope_theta)
         v = (X @ lw["wv"].T).reshape(T, shape.n_kv_heads, hd)
-        cache.K[l, pos0:pos0 + T] = k
-        cache.V[l, pos0:pos0 + T] = v
+        cache.K[l, pos0:pos0 + T] = cache.store(k)
+        cache.V[l, pos0:pos0 + T] = cache.store(v)
         a = attend_rows(q, cache.K[l, :pos0 + T], cache.V[l, :pos0 + T], pos,
                         shape.n_heads, shape.n_kv_heads)
         H = H + a @ lw["wo"].T

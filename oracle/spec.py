@@ -56,10 +56,10 @@ def _dist(z64, temperature: float):
 
 
 class Row:
-    def __init__(self, shape_d: M.Shape, shape_b: M.Shape, max_len: int):
+    def __init__(self, shape_d: M.Shape, shape_b: M.Shape, max_len: int, kv_dtype: str = "f64"):
         self.tokens: list[int] = []
-        self.base = M.KVCache(shape_b, max_len)
-        self.draft = M.KVCache(shape_d, max_len)
+        self.base = M.KVCache(shape_b, max_len, kv_dtype)
+        self.draft = M.KVCache(shape_d, max_len, kv_dtype)
         self.draft_len = 0
         self.phase = 0
         # per-phase records (for parity checks against the CUDA path)
@@ -76,7 +76,8 @@ class SpecDecoder:
 
     def __init__(self, Wd, shape_d: M.Shape, Wb, shape_b: M.Shape,
                  groups=None, k: int = 1, mode: int = M.FULL_LAYER,
-                 max_len: int = 256, calibrate: bool = True, block: bool = False):
+                 max_len: int = 256, calibrate: bool = True, block: bool = False,
+                 kv_dtype: str = "f64"):
         if shape_d.vocab != shape_b.vocab:
             raise ValueError("draft and base must share one vocabulary")
         self.Wd, self.sd, self.Wb, self.sb = Wd, shape_d, Wb, shape_b
@@ -89,13 +90,15 @@ class SpecDecoder:
         # as one block forward instead of token by token: the same model,
         # fast enough for prompts of thousands of tokens
         self.block = block
+        # storage precision of both models' K/V caches ("f64" or "bf16")
+        self.kv_dtype = kv_dtype
         self.rows: list[Row] = []
 
     # -------------------------------------------------------------- stages
     def prefill(self, prompts):
         self.rows = []
         for prompt in prompts:
-            r = Row(self.sd, self.sb, self.max_len)
+            r = Row(self.sd, self.sb, self.max_len, self.kv_dtype)
             r.tokens = [int(t) for t in prompt]
             if self.block:
                 M.forward_block(self.Wb, self.sb, r.tokens[:-1], 0, r.base, logit_rows=[])

@@ -35,8 +35,10 @@ class Pair:
                         max_gamma, mode, None if groups is None else starts_of(groups))
 
     def oracle(self, k=1, mode=ES_FULL_LAYER, groups=None, max_len=256, calibrate=True):
+        # a bf16 pair keeps its K/V cache in bf16 on both sides
         return spec.SpecDecoder(self.Wd, self.shape_d, self.Wb, self.shape_b, groups=groups,
-                                k=k, mode=MODES[mode], max_len=max_len, calibrate=calibrate)
+                                k=k, mode=MODES[mode], max_len=max_len, calibrate=calibrate,
+                                kv_dtype="bf16" if self.dtype == "bf16" else "f64")
 
 
 def rel_l2(a, b):

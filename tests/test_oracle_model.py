@@ -296,3 +296,43 @@ def test_set_layers_match_exact_layers_on_set_input(mode):
             x = _exact_on(_variant(Wd, l, "wo"), sd, l, x + A[l], pos, copy.deepcopy(base))
         want = x
     assert np.allclose(out, want, rtol=1e-12, atol=1e-14)
+
+
+def test_round_bf16_matches_the_library_conversion_and_ties_to_even():
+    """round_bf16 is float32 rounding followed by round-to-nearest-even to
+    8 significant bits: equal to torch's bfloat16 conversion of the float32
+    value, with the halfway cases going to the even neighbour."""
+    import torch
+    r = np.random.default_rng(5)
+    x = np.concatenate([r.normal(size=4000) * 10.0 ** r.integers(-6, 6, size=4000),
+                        [0.0, -0.0, 1.0, -3.5, 65504.0, 1e-40]])
+    want = torch.tensor(x.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(M.round_bf16(x), want)
+    ulp = 2.0 ** -7
+    assert M.round_bf16(1 + ulp / 2) == 1.0                 # tie, 1.0 is even
+    assert M.round_bf16(1 + 3 * ulp / 2) == 1 + 2 * ulp     # tie, 1 + 2 ulp is even
+    assert M.round_bf16(-(1 + 3 * ulp / 2)) == -(1 + 2 * ulp)
+    assert M.round_bf16(1 + ulp / 2 + 1e-6) == 1 + ulp      # above the tie
+
+
+def test_bf16_cache_stores_rounded_entries_that_the_forward_reads():
+    Wd, sd, _, _ = tiny_pair(6, std=0.2)
+    toks = [4, 8, 15, 16, 23, 42]
+    c64, c16 = M.KVCache(sd, 8), M.KVCache(sd, 8, "bf16")
+    z64 = [M.forward_exact(Wd, sd, t, p, c64) for p, t in enumerate(toks)]
+    z16 = [M.forward_exact(Wd, sd, t, p, c16) for p, t in enumerate(toks)]
+    n = len(toks)
+    assert np.array_equal(M.round_bf16(c16.K[:, :n]), c16.K[:, :n])
+    assert np.array_equal(M.round_bf16(c16.V[:, :n]), c16.V[:, :n])
+    # layer 0 at the first position sees only the embedding: its entries are
+    # the rounded float64 ones
+    assert np.array_equal(c16.K[0, 0], M.round_bf16(c64.K[0, 0]))
+    assert np.array_equal(c16.V[0, 0], M.round_bf16(c64.V[0, 0]))
+    # later logits move by about the bf16 rounding of K/V, no more
+    d = np.max(np.abs(np.array(z16) - np.array(z64)))
+    assert 0 < d < 2e-2 * np.max(np.abs(z64))
+    # the block forward stores the same rounded entries
+    cb = M.KVCache(sd, 8, "bf16")
+    zb = M.forward_block(Wd, sd, toks, 0, cb)
+    assert np.max(np.abs(zb - np.array(z16))) < 1e-9
+    assert np.max(np.abs(cb.K[:, :n] - c16.K[:, :n])) <= 2.0 ** -8 * np.max(np.abs(c16.K[:, :n]))
