@@ -1,6 +1,7 @@
 // libeasyspec: host runtime and C ABI for EasySpec layer-parallel
 // speculative decoding on one B300.  See include/easyspec.h for the contract.
-#include <cublas_v2.h>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -21,6 +22,7 @@
 
 #include "../../include/easyspec.h"
 #include "kernels.cuh"
+#include "tcgemm.cuh"
 
 using namespace es;
 
@@ -47,14 +49,17 @@ struct ArgError { std::string msg; es_status st; };
 struct Layer { const void *an, *wq, *wk, *wv, *wo, *mn, *wg, *wu, *wd; };
 
 // One kernel launch of a planned forward pass.
-enum RecKind { R_GV = 0, R_GEMM = 1, R_NORM = 2, R_ATTN = 3 };
+enum RecKind { R_GV = 0, R_GEMM = 1, R_NORM = 2, R_ATTN = 3, R_TC = 4 };
 struct Rec {
     int kind = R_GV;
     const char* name = "";
     double bytes = 0;          // algorithmic bytes (weights + activations), 0 if not modelled
     const GvLaunch* gv = nullptr;           // device copy (after upload)
     std::shared_ptr<GvLaunch> host;         // host copy while the plan is built
-    std::shared_ptr<GvLaunch> gemm_ops;     // many-row passes: the ops, kept on the host
+    std::shared_ptr<TcLaunch> tc_host;      // many-row bf16 pass: tensor-core descriptor on the host
+    const TcLaunch* tc = nullptr;           // its device copy
+    SplitArgs split{};                      // the pass's activation planes
+    int split_grid = 0;
     bool bf16 = false;                      // weights are bf16
     int nw = 8;                             // tensor-core weight pass: warps per CTA (8 or 16)
     int grid = 0, smem = 0, M = 0, ntiles64 = 0;
@@ -96,14 +101,13 @@ struct Graph { cudaGraphExec_t exec = nullptr; int64_t kernels = 0; };
 struct es_ctx {
     es_config cfg{};
     Model md, mb;
-    // many-row bf16 passes (prompt prefill, batches past 8 rows): cuBLAS
-    // tensor-core GEMMs on hi/lo activation planes
-    cublasHandle_t blas = nullptr;
-    void* blas_ws = nullptr;
-    size_t blas_ws_bytes = 0;
-    bf16* tc_x = nullptr;                     // stacked planes [hi; lo] of one source, [2M][K]
-    float *tc_g = nullptr, *tc_u = nullptr;   // [2M][Nc] products (gate / up, or the op's)
-    size_t tc_cap = 0;                        // floats in tc_g and in tc_u
+    // many-row bf16 passes (prompt prefill, batches past 8 rows): the
+    // tcgen05 kernel on hi/lo activation planes
+    bf16* tc_x = nullptr;          // planes of a pass's sources, [2][M][K] each
+    size_t tc_x_elems = 0;
+    float* tc_scratch = nullptr;   // partial accumulators of split tiles
+    size_t tc_scratch_floats = 0;
+    int* tc_counters = nullptr;    // their arrival counters
     cudaStream_t st = nullptr;
     bool own_stream = false;
     int dev = 0, num_sms = 148;
@@ -484,8 +488,203 @@ Rec finish_gv(es_ctx* c, GvBuild& b, const char* name) {
     return r;
 }
 
+// ------------------------------------------------------------------ many-row tensor-core passes
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (no link against libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        CK(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q));
+        if (q != cudaDriverEntryPointSuccess || !p) arg_fail(ES_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+        fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    }
+    return fn;
+}
+
+// Tiled bf16 tensor map with the 128-byte swizzle and zero fill outside the
+// tensor: rank 2 or 3, dims[0] innermost (elements), strides in bytes of
+// dims 1.., box in elements.
+void encode_map(TcMap* out, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                const uint32_t* box) {
+    static_assert(sizeof(TcMap) == sizeof(CUtensorMap), "tensor map size");
+    cuuint64_t gd[3], gs[2];
+    cuuint32_t bx[3], es[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) { gd[i] = dims[i]; bx[i] = box[i]; }
+    for (int i = 0; i + 1 < rank; ++i) gs[i] = strides[i];
+    const CUresult r = tensor_map_encoder()(reinterpret_cast<CUtensorMap*>(out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                            (cuuint32_t)rank, const_cast<void*>(base), gd, gs, bx, es,
+                                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) arg_fail(ES_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+}
+
+// Dynamic shared memory of one CTA alone on an SM (227 KB per CTA, less
+// the kernel's 1 KB of static shared memory) and the share that still lets
+// two CTAs sit on one SM (228 KB per SM).
+constexpr int TC_SMEM_ONE = 226 * 1024;
+constexpr int TC_SMEM_TWO = 110 * 1024;
+
+// A many-row bf16 weight pass: the ops of `b` become one tensor-core launch
+// (tc_gemm_kernel) preceded by one launch that writes the hi/lo planes of
+// its activation sources.
+Rec finish_tc(es_ctx* c, GvBuild& b, const char* name) {
+    const GvLaunch& G = *b.L;
+    auto T = std::make_shared<TcLaunch>();
+    memset(T.get(), 0, sizeof(TcLaunch));
+    TcLaunch& L = *T;
+    const int M = G.M;
+    L.M = M;
+    L.rc = (M + TC_MAXN - 1) / TC_MAXN;
+    L.npad = ((M + L.rc - 1) / L.rc + 15) / 16 * 16;
+    Rec r;
+    r.kind = R_TC;
+    r.name = name;
+    r.M = M;
+    // activation sources -> planes in tc_x, one 3-D map each: [2][M][K]
+    SplitArgs& sa = r.split;
+    memset(&sa, 0, sizeof sa);
+    sa.M = M;
+    int src_of_xs[GV_MAX_XS];
+    for (int i = 0; i < GV_MAX_XS; ++i) src_of_xs[i] = -1;
+    size_t off = 0;
+    double wbytes = 0, xbytes = 0, ybytes = 0;
+    for (int si = 0; si < G.nops; ++si) {
+        const GvOp& o = G.ops[si];
+        for (int j = 0; j < o.nseg; ++j) {
+            const int xs = G.segs[o.seg0 + j].xs;
+            if (src_of_xs[xs] >= 0) continue;
+            const GvXSrc& x = G.xs[xs];
+            if (x.kind != XS_RAW) arg_fail(ES_ERR_ARG, "internal: many-row pass with a normalised source");
+            if (x.K % 8) arg_fail(ES_ERR_ARG, "bf16 weight rows must be a multiple of 8 elements (K = %d)", x.K);
+            const int i = sa.nsrc++;
+            if (i >= TC_MAX_SRCS) arg_fail(ES_ERR_ARG, "too many activation sources in one pass");
+            src_of_xs[xs] = i;
+            off = (off + 127) & ~(size_t)127;  // 256-byte aligned planes
+            if (off + 2 * (size_t)M * x.K > c->tc_x_elems)
+                arg_fail(ES_ERR_ARG, "internal: activation planes exceed their buffer");
+            sa.src[i] = x.src; sa.dst[i] = c->tc_x + off; sa.ld[i] = x.ld; sa.rs[i] = x.row_stride;
+            sa.ro[i] = x.row_off; sa.K[i] = x.K;
+            sa.item0[i + 1] = sa.item0[i] + M * (x.K / 4);
+            const uint64_t dims[3] = {(uint64_t)x.K, (uint64_t)M, 2};
+            const uint64_t strides[2] = {(uint64_t)x.K * 2, (uint64_t)M * x.K * 2};
+            const uint32_t box[3] = {TC_BK, (uint32_t)L.npad, 2};
+            encode_map(&L.maps[TC_MAX_SEGS + i], sa.dst[i], 3, dims, strides, box);
+            off += 2 * (size_t)M * x.K;
+            xbytes += (double)M * x.K * 4;
+        }
+    }
+    r.split_grid = std::max(1, std::min(4 * c->num_sms, (sa.item0[sa.nsrc] + 255) / 256));
+    // ops and segments (one weight map per segment)
+    int nseg = 0;
+    double work = 0;
+    int tiles_all = 0;
+    for (int oi = 0; oi < G.nops; ++oi) {
+        const GvOp& go = G.ops[oi];
+        TcOp& o = L.ops[oi];
+        o.y = go.y; o.add = go.add; o.N = go.N; o.ldy = go.ldy; o.epi = go.epi;
+        o.pair = go.epi == GEPI_SWIGLU;
+        if (o.pair && (go.nseg != 2 || G.segs[go.seg0].set != 0 || G.segs[go.seg0 + 1].set != 1 ||
+                       G.segs[go.seg0].xs != G.segs[go.seg0 + 1].xs))
+            arg_fail(ES_ERR_ARG, "internal: a SwiGLU op needs one gate and one up segment on one source");
+        o.seg0 = nseg; o.nseg = go.nseg; o.nkb = 0;
+        for (int j = 0; j < go.nseg; ++j) {
+            const GvSeg& g = G.segs[go.seg0 + j];
+            if (!o.pair && g.set != 0) arg_fail(ES_ERR_ARG, "internal: second accumulator outside SwiGLU");
+            if (nseg >= TC_MAX_SEGS) arg_fail(ES_ERR_ARG, "too many weight segments in one pass");
+            TcSeg& t = L.segs[nseg];
+            t.wmap = nseg; t.src = src_of_xs[g.xs]; t.K = g.K; t.nkb = (g.K + TC_BK - 1) / TC_BK;
+            t.kb0 = o.pair ? 0 : o.nkb;
+            if (!o.pair || j == 0) o.nkb += t.nkb;
+            const uint64_t dims[2] = {(uint64_t)g.K, (uint64_t)go.N};
+            const uint64_t strides[1] = {(uint64_t)g.K * 2};
+            const uint32_t box[2] = {TC_BK, TC_BM};
+            encode_map(&L.maps[nseg], g.W, 2, dims, strides, box);
+            wbytes += (double)go.N * g.K * 2;
+            ++nseg;
+        }
+        o.ntiles = (go.N + TC_BM - 1) / TC_BM;
+        tiles_all += o.ntiles * L.rc;
+        work += (double)o.ntiles * L.rc * o.nkb * (o.pair ? 2 : 1);
+        ybytes += (double)M * go.N * 4 * (go.epi == GEPI_ACC ? 2 : go.epi == GEPI_ACC_ADD ? 3 : 1);
+    }
+    L.nops = G.nops;
+    L.any_pair = 0;
+    for (int oi = 0; oi < L.nops; ++oi) L.any_pair |= L.ops[oi].pair;
+    // stages: two CTAs per SM when three stages fit in half the shared memory
+    L.stage_bytes = TC_BM * TC_BK * 2 * (L.any_pair ? 2 : 1) + 2 * L.npad * TC_BK * 2;
+    int ctas_per_sm = 1;
+    if (3 * L.stage_bytes + 1024 <= TC_SMEM_TWO) {
+        ctas_per_sm = 2;
+        L.stages = std::min(8, (TC_SMEM_TWO - 1024) / L.stage_bytes);
+    } else {
+        L.stages = std::min(8, (TC_SMEM_ONE - 1024) / L.stage_bytes);
+    }
+    if (L.stages < 2) arg_fail(ES_ERR_ARG, "internal: tensor-core stage of %d bytes too large", L.stage_bytes);
+    const int cols = L.npad * (L.any_pair ? 2 : 1);
+    L.tmem_cols = 32;
+    while (L.tmem_cols < cols) L.tmem_cols *= 2;
+    // k-ranges: when the tiles cannot fill the SMs, cut each tile's k-blocks
+    // into ranges of about work / slots k-blocks, no more units than slots
+    const int slots = c->num_sms * ctas_per_sm;
+    auto assign = [&](int q) {
+        int units = 0, ctr = 0, slot = 0;
+        for (int oi = 0; oi < L.nops; ++oi) {
+            TcOp& o = L.ops[oi];
+            const int w = o.pair ? 2 : 1;
+            o.splits = q <= 0 ? 1 : std::max(1, std::min(o.nkb, (o.nkb * w + q - 1) / q));
+            o.kbps = (o.nkb + o.splits - 1) / o.splits;
+            o.splits = (o.nkb + o.kbps - 1) / o.kbps;
+            o.unit0 = units;
+            units += o.ntiles * L.rc * o.splits;
+            o.tile0 = ctr;
+            o.slot0 = slot;
+            if (o.splits > 1) {
+                ctr += o.ntiles * L.rc;
+                slot += o.ntiles * L.rc * o.splits;
+            }
+        }
+        L.nunits = units;
+        return std::make_pair(ctr, slot);
+    };
+    // A range streams at least max(4, npad / 8) k-blocks of weights (64 KB
+    // per 16 activation rows), so the partial it stores for the tile's last
+    // unit to add up (npad x 128 floats per accumulator) is at most a
+    // quarter of the weight bytes it read.
+    std::pair<int, int> used = assign(0);
+    if (tiles_all < slots) {
+        const int kb_min = std::max(4, L.npad / 8);
+        int q = std::max(kb_min, (int)std::ceil(work / slots));
+        used = assign(q);
+        const size_t slot_floats = (size_t)(L.any_pair ? 2 : 1) * L.npad * TC_BM;
+        while (L.nunits > slots || used.first > TC_COUNTERS ||
+               (size_t)used.second * slot_floats > c->tc_scratch_floats) {
+            ++q;
+            used = assign(q);
+        }
+    }
+    r.grid = L.nunits;
+    r.smem = L.stages * L.stage_bytes + 1024;
+    r.bytes = wbytes + xbytes + ybytes;
+    r.tc_host = T;
+    return r;
+}
+
 void upload_plan(es_ctx* c, Plan& p) {
     for (Rec& r : p.recs) {
+        if (r.tc_host) {
+            const size_t bytes = sizeof(TcLaunch);
+            const size_t at = (c->arena_used + 255) & ~(size_t)255;
+            if (at + bytes > c->arena_cap) arg_fail(ES_ERR_OOM, "launch descriptor arena exhausted");
+            CK(cudaMemcpy(c->arena + at, r.tc_host.get(), bytes, cudaMemcpyHostToDevice));
+            c->arena_used = at + bytes;
+            r.tc = reinterpret_cast<const TcLaunch*>(c->arena + at);
+            r.tc_host.reset();
+            continue;
+        }
         if (!r.host) continue;
         const size_t bytes = sizeof(GvLaunch);
         const size_t at = (c->arena_used + 255) & ~(size_t)255;
@@ -493,7 +692,6 @@ void upload_plan(es_ctx* c, Plan& p) {
         CK(cudaMemcpy(c->arena + at, r.host.get(), bytes, cudaMemcpyHostToDevice));
         c->arena_used = at + bytes;
         r.gv = reinterpret_cast<const GvLaunch*>(c->arena + at);
-        if (r.kind == R_GEMM) r.gemm_ops = r.host;
         r.host.reset();
     }
 }
@@ -594,7 +792,8 @@ Plan build_forward(es_ctx* c, Model& m, const std::vector<std::vector<int>>& gro
         return b.source(buf, m.d, m.d);
     };
     auto push_gv = [&](GvBuild& b, const char* name) {
-        P.recs.push_back(finish_gv(c, b, label(m, name)));
+        if (!fast && m.esz == 2) P.recs.push_back(finish_tc(c, b, label(m, name)));
+        else P.recs.push_back(finish_gv(c, b, label(m, name)));
         writer = (int)P.recs.size() - 1;
     };
     auto raw = [&](GvBuild& b, const float* p, int K) { return b.source(p, K, K); };
@@ -708,78 +907,6 @@ std::vector<std::vector<int>> default_sets(int L, int k) {
 }
 
 // ------------------------------------------------------------------ launches
-void blas_check(cublasStatus_t st, int line) {
-    if (st != CUBLAS_STATUS_SUCCESS) arg_fail(ES_ERR_CUDA, "cuBLAS status %d at line %d", (int)st, line);
-}
-
-// A many-row weight pass with bf16 weights: for each op and segment, the
-// segment's activations are split into bf16 hi/lo planes and
-// y (+)= W . hi + W . lo runs as two cuBLAS GEMMs (bf16 in, float32
-// accumulate and out, tensor cores); residual adds and SwiGLU follow as one
-// elementwise kernel.  Row-major y[M][N] = x[M][K] . W[N][K]^T is the
-// column-major product W^T(K x N, transposed) . x(K x M).
-void gemm_many_rows(es_ctx* c, const Rec& r) {
-    const GvLaunch& L = *r.gemm_ops;
-    const int M = L.M;
-    cudaEvent_t ev0 = nullptr, ev1 = nullptr;
-    if (c->profiling) {
-        if (c->prof_pool_used == c->prof_pool.size()) {
-            cudaEvent_t x, y;
-            CK(cudaEventCreate(&x));
-            CK(cudaEventCreate(&y));
-            c->prof_pool.emplace_back(x, y);
-        }
-        ev0 = c->prof_pool[c->prof_pool_used].first;
-        ev1 = c->prof_pool[c->prof_pool_used].second;
-        c->prof_pool_used++;
-        CK(cudaEventRecord(ev0, c->st));
-    }
-    blas_check(cublasSetStream(c->blas, c->st), __LINE__);
-    // Both planes of a source go through one GEMM as 2M activation rows, so
-    // every weight row is streamed once; the epilogue adds the two halves.
-    // Ops of one pass do not read each other's outputs, so a source split for
-    // one op serves the next ones too.
-    int split_xs = -1;
-    const float one = 1.0f, zero = 0.0f;
-    for (int oi = 0; oi < L.nops; ++oi) {
-        const GvOp& o = L.ops[oi];
-        const bool swi = o.epi == GEPI_SWIGLU;
-        float* scr[2] = {c->tc_g, c->tc_u};
-        const int cw = (int)std::min<size_t>((size_t)o.N, c->tc_cap / (2 * (size_t)M));  // columns per chunk
-        for (int n0 = 0; n0 < o.N; n0 += cw) {
-            const int nc = std::min(cw, o.N - n0);
-            bool first[2] = {true, true};
-            for (int si = 0; si < o.nseg; ++si) {
-                const GvSeg& sg = L.segs[o.seg0 + si];
-                const GvXSrc& x = L.xs[sg.xs];
-                if (x.K != sg.K || sg.K % 4) arg_fail(ES_ERR_ARG, "internal: many-row segment width %d", sg.K);
-                if (sg.xs != split_xs) {
-                    const int items = M * (sg.K / 4);
-                    launch(c, "split_hilo", 0.0, split_hilo_kernel,
-                           dim3(std::min(4 * c->num_sms, (items + 255) / 256)), dim3(256), (size_t)0, x.src, x.ld,
-                           x.row_stride, x.row_off, M, sg.K, c->tc_x, c->tc_x + (size_t)M * sg.K);
-                    split_xs = sg.xs;
-                }
-                const int set = sg.set;
-                blas_check(cublasGemmEx(c->blas, CUBLAS_OP_T, CUBLAS_OP_N, nc, 2 * M, sg.K, &one,
-                                        (const bf16*)sg.W + (size_t)n0 * sg.K, CUDA_R_16BF, sg.K, c->tc_x,
-                                        CUDA_R_16BF, sg.K, first[set] ? &zero : &one, scr[set], CUDA_R_32F, nc,
-                                        CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT),
-                           __LINE__);
-                first[set] = false;
-            }
-            const size_t n = (size_t)M * nc;
-            launch(c, "epi_hilo", 0.0, epi_hilo_kernel, dim3((unsigned)std::min<size_t>(4 * c->num_sms, (n + 255) / 256)),
-                   dim3(256), (size_t)0, o.y + n0, o.ldy, o.epi == GEPI_ACC_ADD ? o.add + n0 : nullptr, (int)o.epi,
-                   (const float*)c->tc_g, swi ? (const float*)c->tc_u : nullptr, M, nc);
-        }
-    }
-    if (c->profiling) {
-        CK(cudaEventRecord(ev1, c->st));
-        c->prof_pending.push_back(ProfRec{r.name, r.bytes, ev0, ev1});
-    }
-}
-
 template <typename T>
 void run_rec(es_ctx* c, const Rec& r) {
     switch (r.kind) {
@@ -806,12 +933,13 @@ void run_rec(es_ctx* c, const Rec& r) {
             }
             break;
         case R_GEMM:
-            if constexpr (std::is_same<T, bf16>::value) {
-                gemm_many_rows(c, r);
-            } else {
-                launch(c, "gemm_simt", r.bytes, gemm_kernel<T>, dim3(r.ntiles64, (r.M + GB - 1) / GB),
-                       dim3(256), (size_t)0, r.gv);
-            }
+            launch(c, "gemm_simt", r.bytes, gemm_kernel<T>, dim3(r.ntiles64, (r.M + GB - 1) / GB),
+                   dim3(256), (size_t)0, r.gv);
+            break;
+        case R_TC:
+            launch(c, "split_planes", 0.0, split_planes_kernel, dim3(r.split_grid), dim3(256), (size_t)0, r.split);
+            launch(c, r.name, r.bytes, tc_gemm_kernel, dim3(r.grid), dim3(TC_THREADS), (size_t)r.smem, r.tc,
+                   c->tc_scratch, c->tc_counters, c->status + 1);
             break;
         case R_NORM:
             launch(c, r.name, 0.0, norm_kernel<T>, dim3(r.M), dim3(256), (size_t)0, r.norm);
@@ -897,11 +1025,17 @@ void prof_collect(es_ctx* c);
 void check_status(es_ctx* c) {
     // reads the device status word (call after a stream sync)
     if (c->profiling) prof_collect(c);
-    int s = 0;
-    CK(cudaMemcpy(&s, c->status, sizeof(int), cudaMemcpyDeviceToHost));
-    if (s) {
+    int st[2] = {0, 0};
+    CK(cudaMemcpy(st, c->status, sizeof st, cudaMemcpyDeviceToHost));
+    if (st[1]) {
+        // a tensor-core pass gave up a bounded wait: its results are not
+        // valid, and the context is not usable any more
+        c->poisoned = true;
+        arg_fail(ES_ERR_TIMEOUT, "a device-side wait of a tensor-core weight pass ran out of time (flag 0x%x)", st[1]);
+    }
+    if (st[0]) {
         CK(cudaMemset(c->status, 0, sizeof(int)));
-        arg_fail(ES_ERR_STATE, "device reported invalid rows (status 0x%x): position past max_seq or token out of range", s);
+        arg_fail(ES_ERR_STATE, "device reported invalid rows (status 0x%x): position past max_seq or token out of range", st[0]);
     }
 }
 
@@ -1301,28 +1435,28 @@ es_status easyspec_init(const es_config* cfg, const es_weights* draft, const es_
         c->p_logits = c->dalloc<float>((size_t)Bm * (G + 1) * V);
         c->p_probs = c->dalloc<float>((size_t)Bm * (G + 1) * V);
         c->prm = c->dalloc<RunParams>(1);
-        c->status = c->dalloc<int>(1);
+        c->status = c->dalloc<int>(2);  // [0] invalid rows, [1] a bounded device wait ran out
         c->arena_cap = (size_t)64 << 20;
         c->arena = c->dalloc<char>(c->arena_cap);
         c->gv_scratch = c->dalloc<float>(std::max(GV_SCRATCH_FLOATS, GVM_SCRATCH_FLOATS));
         if (c->md.dtype == ES_DTYPE_BF16 || c->mb.dtype == ES_DTYPE_BF16) {
-            // many-row bf16 passes: cuBLAS with a fixed workspace (so they can
-            // be captured in CUDA graphs) and the hi/lo / SwiGLU buffers
-            size_t rows = 0, kmax = 0, fmax = 0;
+            // many-row bf16 passes: activation planes of the widest pass
+            // (a set's K-concatenated o/down sources, or its 2 x n
+            // normalised inputs) and the partials of split tiles
+            size_t per_row = 0, rows = 0;
             for (const Model* mm : {&c->md, &c->mb}) {
                 rows = std::max(rows, (size_t)mm->Mw);
-                kmax = std::max({kmax, (size_t)mm->d, (size_t)mm->qd, (size_t)mm->F});
-                fmax = std::max({fmax, (size_t)mm->F, (size_t)mm->d, (size_t)mm->qd});
+                const size_t n = (size_t)mm->slots;
+                per_row = std::max({per_row, n * (size_t)(mm->qd + mm->F), 2 * n * (size_t)mm->d,
+                                    (size_t)mm->F, (size_t)mm->qd, (size_t)mm->d});
             }
-            if (cublasCreate(&c->blas) != CUBLAS_STATUS_SUCCESS) arg_fail(ES_ERR_CUDA, "cublasCreate failed");
-            c->blas_ws_bytes = (size_t)32 << 20;
-            c->blas_ws = c->dalloc<char>(c->blas_ws_bytes);
-            blas_check(cublasSetWorkspace(c->blas, c->blas_ws, c->blas_ws_bytes), __LINE__);
-            blas_check(cublasSetStream(c->blas, c->st), __LINE__);
-            c->tc_x = c->dalloc<bf16>(2 * rows * kmax);
-            c->tc_cap = 2 * rows * fmax;
-            c->tc_g = c->dalloc<float>(c->tc_cap);
-            c->tc_u = c->dalloc<float>(c->tc_cap);
+            c->tc_x_elems = 2 * rows * per_row + (size_t)128 * 2 * TC_MAX_SRCS;
+            c->tc_x = c->dalloc<bf16>(c->tc_x_elems);
+            c->tc_scratch_floats = (size_t)c->num_sms * 2 * 2 * TC_BM * TC_MAXN;
+            c->tc_scratch = c->dalloc<float>(c->tc_scratch_floats);
+            c->tc_counters = c->dalloc<int>(TC_COUNTERS);
+            CK(cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM_ONE));
+            tensor_map_encoder();
         }
         c->gv_counters = c->dalloc<int>(GV_COUNTERS);
         c->gv_done = c->dalloc<int>(1);
@@ -1664,7 +1798,6 @@ void easyspec_destroy(es_ctx* c) {
     if (c->h_prm) cudaFreeHost(c->h_prm);
     if (c->h_small) cudaFreeHost(c->h_small);
     if (c->cfg.group_starts) delete[] c->cfg.group_starts;
-    if (c->blas) cublasDestroy(c->blas);
     if (c->own_stream) cudaStreamDestroy(c->st);
     delete c;
 }

@@ -1,0 +1,454 @@
+// Many-row weight passes on the fifth-generation tensor cores (sm_103a):
+// tcgen05.mma with operands staged in shared memory by TMA and the
+// accumulator in tensor memory.
+//
+// A pass with more than 8 activation rows (prompt prefill, the verify of
+// gamma+1 rows per sequence for a batch, calibration of a batch) computes,
+// for every op o of the launch and every output feature n < N_o and
+// activation row r < M,
+//   acc_set[n][r] = sum over the op's segments s of set `set`:
+//                   W_s[n, :] . x_s[r, :]
+// and applies the op's epilogue (STORE, ACC, ACC_ADD, SWIGLU as in the
+// decode weight pass).  Activations arrive as bf16 planes hi = bf16(x),
+// lo = bf16(x - hi) of the float32 rows (written by split_planes_kernel);
+// both planes are multiplied into the same float32 accumulator, so the
+// products keep ~16 significant bits of x with bf16 weights.
+//
+// Swapped operands: the weights are the MMA's A operand (M = 128 weight rows
+// per tile) and the activation rows its B operand (N = the rows, padded to a
+// multiple of 16, at most 256 per row chunk).  The accumulator D[n][r] sits
+// in tensor memory with lane = weight row and column = activation row, so
+// the epilogue thread of lane n writes y[r][n] for consecutive n across a
+// warp: coalesced rows of the row-major output.
+//
+// CTA roles (256 threads): thread 0 issues the TMA loads (weights before
+// griddepcontrol.wait -- they do not depend on the previous kernel --
+// activations after), thread 32 issues the MMAs and commits each stage back
+// to its "empty" barrier, and afterwards all 8 warps read the accumulator
+// (warp w: lanes 32*(w%4).., column half w/4) and run the epilogue.
+//
+// Work split.  A unit is (op, 128-row weight tile, row chunk, range of
+// 64-column k-blocks).  When the tiles alone cannot fill the SMs, each tile's
+// k-blocks are cut into equal ranges; every range stores its partial
+// accumulator in `scratch`, and the last unit of the tile to arrive (an
+// arrival counter, no waiting) adds the partials in range order -- the
+// result does not depend on which unit arrives last -- applies the epilogue
+// and resets the counter.
+//
+// Every wait on an mbarrier is bounded (TC_WAIT_NS of the global timer).  A
+// wait that runs out sets bit 0 of `err`, the CTA stops issuing work, waits
+// (bounded again) for the copies it still has in flight, frees its tensor
+// memory and returns; the host reports ES_ERR_TIMEOUT.
+#pragma once
+#include "common.cuh"
+#include "gemv.cuh"
+
+namespace es {
+
+constexpr int TC_BM = 128;            // weight rows per tile (MMA M)
+constexpr int TC_BK = 64;             // k per stage: one 128-byte swizzle row of bf16
+constexpr int TC_MAXN = 256;          // activation rows per chunk (MMA N)
+constexpr int TC_THREADS = 256;
+constexpr int TC_MAX_OPS = 32;
+constexpr int TC_MAX_SEGS = 64;
+constexpr int TC_MAX_SRCS = 16;
+constexpr int TC_COUNTERS = 16384;    // arrival counters of split tiles
+constexpr unsigned long long TC_WAIT_NS = 2000000000ull;  // 2 s
+
+// A CUtensorMap (128 bytes, 64-byte aligned), filled on the host.
+struct alignas(64) TcMap { unsigned long long w[16]; };
+
+struct TcSeg {
+    int wmap;      // tensor map of the weights W_s [N, K] (box 64 x 128)
+    int src;       // activation source (its planes' tensor map)
+    int K, nkb;    // columns, 64-column k-blocks
+    int kb0;       // first k-block of this segment within its op
+    int pad_[3];
+};
+struct TcOp {
+    float* y; const float* add;
+    int N, ldy, epi, pair;     // pair: SwiGLU, segment seg0 = gate, seg0+1 = up
+    int seg0, nseg, nkb;       // k-blocks over all segments (pair: of one)
+    int ntiles, splits, kbps;  // tiles, k-ranges per tile, k-blocks per range
+    int unit0;                 // first unit of this op
+    int tile0;                 // first arrival counter of this op's tiles
+    int slot0;                 // first partial slot (split ops)
+    int pad_;
+};
+struct TcLaunch {
+    TcMap maps[TC_MAX_SEGS + TC_MAX_SRCS];  // weights, then activation planes
+    TcSeg segs[TC_MAX_SEGS];
+    TcOp ops[TC_MAX_OPS];
+    int nops, nunits, M, rc, npad, stages, stage_bytes, tmem_cols, any_pair, pad_[7];
+};
+static_assert(sizeof(TcLaunch) % 64 == 0, "descriptor keeps its maps 64-byte aligned");
+
+// Activation planes: for source i, rows r*row_stride + row_off of src
+// (leading dimension ld, K columns) become hi/lo bf16 planes
+// dst[0][r][k], dst[1][r][k] ([2][M][K]).
+struct SplitArgs {
+    const float* src[TC_MAX_SRCS];
+    bf16* dst[TC_MAX_SRCS];
+    int ld[TC_MAX_SRCS], rs[TC_MAX_SRCS], ro[TC_MAX_SRCS], K[TC_MAX_SRCS];
+    int item0[TC_MAX_SRCS + 1];  // prefix of M*K/4 items per source
+    int nsrc, M;
+};
+
+__global__ void split_planes_kernel(SplitArgs a) {
+    grid_dep_wait();
+    grid_dep_launch();
+    const int total = a.item0[a.nsrc];
+    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < total; t += gridDim.x * blockDim.x) {
+        int i = 0;
+        while (t >= a.item0[i + 1]) ++i;
+        const int K4 = a.K[i] >> 2, u = t - a.item0[i];
+        const int m = u / K4, k = (u - m * K4) * 4;
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(
+            a.src[i] + (size_t)(m * a.rs[i] + a.ro[i]) * a.ld[i] + k));
+        const __nv_bfloat162 h0 = __floats2bfloat162_rn(v.x, v.y), h1 = __floats2bfloat162_rn(v.z, v.w);
+        const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+        const __nv_bfloat162 l0 = __floats2bfloat162_rn(v.x - f0.x, v.y - f0.y);
+        const __nv_bfloat162 l1 = __floats2bfloat162_rn(v.z - f1.x, v.w - f1.y);
+        const size_t plane = (size_t)a.M * a.K[i];
+        __nv_bfloat162* ph = reinterpret_cast<__nv_bfloat162*>(a.dst[i] + (size_t)m * a.K[i] + k);
+        __nv_bfloat162* pl = reinterpret_cast<__nv_bfloat162*>(a.dst[i] + plane + (size_t)m * a.K[i] + k);
+        ph[0] = h0; ph[1] = h1; pl[0] = l0; pl[1] = l1;
+    }
+}
+
+// ------------------------------------------------------------ PTX wrappers
+ES_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+ES_DEV unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+ES_DEV void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+ES_DEV void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+ES_DEV bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+// Wait for the phase of `parity` to complete, at most TC_WAIT_NS; false
+// (and bit 0 of *err set) when the limit ran out, or when another thread of
+// the CTA gave up (*abort) and `stop_on_abort` is set.
+ES_DEV bool mbar_wait(uint32_t bar, uint32_t parity, int* err, volatile int* abort, bool stop_on_abort = true) {
+    if (mbar_test(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_test(bar, parity)) return true;
+        if ((i & 63) == 0) {
+            if (stop_on_abort && *abort) return false;
+            if (global_ns() - t0 > TC_WAIT_NS) {
+                atomicOr(err, 1);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+ES_DEV void tma_load_2d(uint32_t dst, const TcMap* map, int c0, int c1, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(bar) : "memory");
+}
+ES_DEV void tma_load_3d(uint32_t dst, const TcMap* map, int c0, int c1, int c2, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar) : "memory");
+}
+
+ES_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+ES_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a K-major operand tile whose rows are
+// 128 bytes (64 bf16) in the 128-byte swizzle: 8-row groups 1024 bytes
+// apart (stride byte offset), descriptor version 1, layout SWIZZLE_128B.
+// The tile starts on a 1024-byte boundary; a k16 step inside it advances the
+// start address by 32 bytes.
+ES_DEV uint64_t sw128_desc(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor, kind::f16: float32 accumulator, bf16 A and B, both
+// K-major, M = 128, N = n.
+ES_DEV uint32_t mma_idesc(int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(TC_BM >> 4) << 24);
+}
+ES_DEV void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, int accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
+        ::"r"(tmem_d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
+}
+ES_DEV void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+// 8 consecutive accumulator columns of this thread's lane.
+ES_DEV void tmem_ld8(uint32_t taddr, float* v) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+ES_DEV float tc_epi(int epi, float a, float b, const float* yp, const float* ap) {
+    switch (epi) {
+        case GEPI_SWIGLU: return silu_f(a) * b;
+        case GEPI_STORE: return a;
+        case GEPI_ACC: return __ldcg(yp) + a;
+        default: return __ldcg(yp) + a + __ldcg(ap);
+    }
+}
+
+// ------------------------------------------------------------ the kernel
+__global__ void __launch_bounds__(TC_THREADS, 1)
+tc_gemm_kernel(const TcLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __restrict__ counters,
+               int* __restrict__ err) {
+    extern __shared__ __align__(1024) unsigned char tsm_raw[];
+    __shared__ __align__(8) unsigned long long bars[2 * 8 + 1];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort, s_last;
+    // the dynamic region is aligned to 1024 bytes by hand
+    unsigned char* tsm = tsm_raw + ((1024 - (smem_u32(tsm_raw) & 1023)) & 1023);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const TcLaunch& L = *Lg;
+    const int S = L.stages, npad = L.npad;
+    // ---- which unit
+    const int unit = blockIdx.x;
+    int oi = 0;
+    while (oi + 1 < L.nops && L.ops[oi + 1].unit0 <= unit) ++oi;
+    const TcOp& op = L.ops[oi];
+    const int u = unit - op.unit0;
+    const int split = u % op.splits, tc = u / op.splits;
+    const int chunk = tc % L.rc, tile = tc / L.rc;
+    const int kb_begin = split * op.kbps, kb_end = min(op.nkb, kb_begin + op.kbps);
+    const int nkb = kb_end - kb_begin;
+    const int pair = op.pair;
+    const uint32_t w_bytes = TC_BM * TC_BK * 2;
+    const uint32_t x_bytes = 2u * npad * TC_BK * 2;   // both planes
+    const uint32_t tx_bytes = w_bytes * (pair ? 2 : 1) + x_bytes;
+
+    auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
+    auto empty_bar = [&](int s) { return smem_u32(&bars[8 + s]); };
+    const uint32_t acc_bar = smem_u32(&bars[16]);
+    auto st_w0 = [&](int s) { return smem_u32(tsm + (size_t)s * L.stage_bytes); };
+    auto st_w1 = [&](int s) { return st_w0(s) + w_bytes; };
+    auto st_x = [&](int s) { return st_w0(s) + w_bytes * (L.any_pair ? 2 : 1); };
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(acc_bar, 1);
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "r"(L.tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    volatile int* abort = &s_abort;
+
+    // k-block j of this unit -> segment and its local k-block
+    auto locate = [&](int kb, int* seg) {
+        int s = op.seg0;
+        if (!pair)
+            while (s + 1 < op.seg0 + op.nseg && L.segs[s + 1].kb0 <= kb) ++s;
+        *seg = s;
+        return kb - L.segs[s].kb0;
+    };
+
+    if (tid == 0) {
+        // ---- TMA producer.  The weight tiles of the first stages go out
+        // before the dependency wait; their activation planes after it.
+        const int pre = min(S, nkb);
+        for (int j = 0; j < pre; ++j) {
+            int sg;
+            const int kl = locate(kb_begin + j, &sg);
+            mbar_arrive_tx(full_bar(j), tx_bytes);
+            tma_load_2d(st_w0(j), &L.maps[L.segs[sg].wmap], kl * TC_BK, tile * TC_BM, full_bar(j));
+            if (pair) tma_load_2d(st_w1(j), &L.maps[L.segs[sg + 1].wmap], kl * TC_BK, tile * TC_BM, full_bar(j));
+        }
+        grid_dep_wait();
+        for (int j = 0; j < pre; ++j) {
+            int sg;
+            const int kl = locate(kb_begin + j, &sg);
+            tma_load_3d(st_x(j), &L.maps[TC_MAX_SEGS + L.segs[sg].src], kl * TC_BK, chunk * npad, 0, full_bar(j));
+        }
+        int issued = pre;
+        for (int j = pre; j < nkb; ++j) {
+            const int s = j % S;
+            if (!mbar_wait(empty_bar(s), ((j / S) - 1) & 1, err, abort)) break;
+            int sg;
+            const int kl = locate(kb_begin + j, &sg);
+            mbar_arrive_tx(full_bar(s), tx_bytes);
+            tma_load_2d(st_w0(s), &L.maps[L.segs[sg].wmap], kl * TC_BK, tile * TC_BM, full_bar(s));
+            if (pair) tma_load_2d(st_w1(s), &L.maps[L.segs[sg + 1].wmap], kl * TC_BK, tile * TC_BM, full_bar(s));
+            tma_load_3d(st_x(s), &L.maps[TC_MAX_SEGS + L.segs[sg].src], kl * TC_BK, chunk * npad, 0, full_bar(s));
+            issued = j + 1;
+        }
+        if (*abort) {
+            // let the copies still in flight land before the CTA leaves
+            for (int j = max(0, issued - S); j < issued; ++j) {
+                const unsigned long long t0 = global_ns();
+                while (!mbar_test(full_bar(j % S), (j / S) & 1) && global_ns() - t0 < TC_WAIT_NS) {
+                }
+            }
+        }
+    } else if (tid == 32) {
+        // ---- MMA issuer
+        const uint32_t idesc = mma_idesc(npad);
+        for (int j = 0; j < nkb; ++j) {
+            const int s = j % S;
+            if (!mbar_wait(full_bar(s), (j / S) & 1, err, abort)) break;
+            tc_fence_after();
+            const uint32_t xa = st_x(s), xb = xa + npad * TC_BK * 2;
+#pragma unroll
+            for (int ks = 0; ks < TC_BK / 16; ++ks) {
+                const uint64_t bh = sw128_desc(xa + ks * 32), bl = sw128_desc(xb + ks * 32);
+                const uint64_t a0 = sw128_desc(st_w0(s) + ks * 32);
+                mma_bf16(tmem, a0, bh, idesc, j > 0 || ks > 0);
+                mma_bf16(tmem, a0, bl, idesc, 1);
+                if (pair) {
+                    const uint64_t a1 = sw128_desc(st_w1(s) + ks * 32);
+                    mma_bf16(tmem + npad, a1, bh, idesc, j > 0 || ks > 0);
+                    mma_bf16(tmem + npad, a1, bl, idesc, 1);
+                }
+            }
+            mma_commit(empty_bar(s));
+        }
+        mma_commit(acc_bar);
+    }
+    __syncwarp();
+    grid_dep_wait();
+    grid_dep_launch();
+
+    // ---- epilogue: all warps.  The accumulator barrier completes once every
+    // MMA issued has finished (also after an abort), so the tensor memory is
+    // not freed under a running MMA.
+    bool ok = mbar_wait(acc_bar, 0, err, abort, false);
+    ok = __all_sync(0xffffffffu, ok) && nkb > 0;
+    __syncthreads();
+    ok = ok && !*abort;
+    tc_fence_after();
+    const int lq = warp & 3, half = warp >> 2;
+    const int nl = lq * 32 + lane;              // accumulator lane = weight row in the tile
+    const int n = tile * TC_BM + nl;
+    const int cw = npad / 2;                    // columns per warp half (multiple of 8)
+    const uint32_t tl = tmem + ((uint32_t)(lq * 32) << 16);
+    const int r0 = chunk * npad;
+    if (ok) {
+        if (op.splits == 1) {
+            for (int c = half * cw; c < half * cw + cw; c += 8) {
+                float a[8], b[8];
+                tmem_ld8(tl + c, a);
+                if (pair) tmem_ld8(tl + npad + c, b);
+                if (n < op.N) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int r = r0 + c + i;
+                        if (r < L.M) {
+                            float* yp = op.y + (size_t)r * op.ldy + n;
+                            *yp = tc_epi(op.epi, a[i], pair ? b[i] : 0.f, yp,
+                                         op.add ? op.add + (size_t)r * op.ldy + n : nullptr);
+                        }
+                    }
+                }
+            }
+        } else {
+            // partial of this k-range: [acc][column][lane] at its slot
+            const int nacc = pair ? 2 : 1;
+            const size_t slot_floats = (size_t)nacc * npad * TC_BM;
+            const int tslot = op.slot0 + tc * op.splits;   // slot of the tile's range 0
+            float* part = scratch + (size_t)(tslot + split) * slot_floats;
+            for (int c = half * cw; c < half * cw + cw; c += 8) {
+                float a[8], b[8];
+                tmem_ld8(tl + c, a);
+                if (pair) tmem_ld8(tl + npad + c, b);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    part[(size_t)(c + i) * TC_BM + nl] = a[i];
+                    if (pair) part[(size_t)(npad + c + i) * TC_BM + nl] = b[i];
+                }
+            }
+            __syncthreads();
+            const int old = cta_arrive(counters + op.tile0 + tc);
+            if (tid == 0) s_last = old == op.splits - 1;
+            __syncthreads();
+            if (s_last) {
+                // sum the ranges' partials in range order, four features per
+                // thread and four ranges' loads in flight at a time
+                if (tid == 0) counters[op.tile0 + tc] = 0;
+                const float* p0 = scratch + (size_t)tslot * slot_floats;
+                const int n4 = npad * TC_BM / 4;
+                for (int e = tid; e < n4; e += TC_THREADS) {
+                    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+                    const float4* q0 = reinterpret_cast<const float4*>(p0) + e;
+                    const size_t sf4 = slot_floats / 4, acc1 = (size_t)npad * TC_BM / 4;
+                    auto add4 = [](float4& x, const float4& y) { x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w; };
+                    int sp = 0;
+                    for (; sp + 4 <= op.splits; sp += 4) {
+                        float4 v[4], w[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) v[i] = __ldcg(q0 + (sp + i) * sf4);
+                        if (pair) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) w[i] = __ldcg(q0 + (sp + i) * sf4 + acc1);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            add4(a, v[i]);
+                            if (pair) add4(b, w[i]);
+                        }
+                    }
+                    for (; sp < op.splits; ++sp) {
+                        add4(a, __ldcg(q0 + sp * sf4));
+                        if (pair) add4(b, __ldcg(q0 + sp * sf4 + acc1));
+                    }
+                    const int c = e / (TC_BM / 4), nl0 = (e % (TC_BM / 4)) * 4;
+                    const int r = r0 + c;
+                    if (r >= L.M) continue;
+                    const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int nn = tile * TC_BM + nl0 + i;
+                        if (nn >= op.N) break;
+                        float* yp = op.y + (size_t)r * op.ldy + nn;
+                        *yp = tc_epi(op.epi, av[i], bv[i], yp, op.add ? op.add + (size_t)r * op.ldy + nn : nullptr);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(L.tmem_cols) : "memory");
+}
+
+}  // namespace es

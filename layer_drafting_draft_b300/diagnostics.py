@@ -46,9 +46,11 @@ from .easyspec import ES_ATTN_ONLY, ES_FULL_LAYER, EasySpec
 
 
 def fuzzy_kv_error(g: EasySpec, sd: dict, prompt: np.ndarray, k: int, gamma: int, phases: int,
-                   temperature: float = 0.0, seed: int = 0) -> dict:
+                   temperature: float = 0.0, seed: int = 0, trace: list | None = None) -> dict:
     """Per-layer {cos_k, cos_v, rel_k, rel_v, n} over `phases` phases of one
-    sequence (prompt [1, P]); g must hold that single sequence's context."""
+    sequence (prompt [1, P]); g must hold that single sequence's context.
+    When `trace` is a list, each phase appends (draft tokens, accepted
+    count, committed tokens), so the run can be replayed elsewhere."""
     L, Hkv, hd = sd["n_layers"], sd["n_kv_heads"], sd["head_dim"]
     g.easyspec_prefill(prompt)
     n = prompt.shape[1]          # committed tokens
@@ -56,7 +58,7 @@ def fuzzy_kv_error(g: EasySpec, sd: dict, prompt: np.ndarray, k: int, gamma: int
     count = 0
     pending = None               # (positions with fuzzy entries, their K/V per layer)
     for ph in range(phases + 1):
-        g.draft_step(k, gamma, temperature, seed + ph)   # calibration of the previous phase's commits
+        drafts = g.draft_step(k, gamma, temperature, seed + ph)   # calibration of the previous phase's commits
         if pending is not None:
             pos, fuzzy = pending
             for l in range(L):
@@ -79,8 +81,10 @@ def fuzzy_kv_error(g: EasySpec, sd: dict, prompt: np.ndarray, k: int, gamma: int
         for l in range(L):
             kk, vv = g.es_read_kv(0, l, 0, n + gamma - 1, Hkv, hd)
             snap[l] = (kk[n:], vv[n:])
-        acc, _ = g.verify_step(temperature, seed + ph, gamma)
+        acc, toks = g.verify_step(temperature, seed + ph, gamma)
         a = int(acc[0])
+        if trace is not None:
+            trace.append((drafts[0].tolist(), a, toks[0, : a + 1].tolist()))
         kept = fuzzy_pos[: min(a, gamma - 1)]      # accepted drafts that carried a fuzzy entry
         if kept:
             pending = (kept, {l: (snap[l][0][: len(kept)], snap[l][1][: len(kept)]) for l in range(L)})
