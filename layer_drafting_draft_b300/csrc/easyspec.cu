@@ -59,7 +59,7 @@ struct Rec {
     std::shared_ptr<TcLaunch> tc_host;      // many-row bf16 pass: tensor-core descriptor on the host
     const TcLaunch* tc = nullptr;           // its device copy
     SplitArgs split{};                      // the pass's activation planes
-    int split_grid = 0;
+    int split_grid = 0, cluster = 1;
     bool bf16 = false;                      // weights are bf16
     int nw = 8;                             // tensor-core weight pass: warps per CTA (8 or 16)
     int grid = 0, smem = 0, M = 0, ntiles64 = 0;
@@ -105,9 +105,6 @@ struct es_ctx {
     // tcgen05 kernel on hi/lo activation planes
     bf16* tc_x = nullptr;          // planes of a pass's sources, [2][M][K] each
     size_t tc_x_elems = 0;
-    float* tc_scratch = nullptr;   // partial accumulators of split tiles
-    size_t tc_scratch_floats = 0;
-    int* tc_counters = nullptr;    // their arrival counters
     cudaStream_t st = nullptr;
     bool own_stream = false;
     int dev = 0, num_sms = 148;
@@ -182,8 +179,8 @@ namespace {
 
 // ------------------------------------------------------------------ launch helper
 template <typename... KArgs, typename... Args>
-void launch(es_ctx* c, const char* name, double bytes, void (*kern)(KArgs...), dim3 grid,
-            dim3 block, size_t smem, Args... args) {
+void launch_cl(es_ctx* c, const char* name, double bytes, int cluster, void (*kern)(KArgs...), dim3 grid,
+               dim3 block, size_t smem, Args... args) {
     if (grid.x == 0 || grid.y == 0 || grid.z == 0) return;
     cudaEvent_t ev0 = nullptr, ev1 = nullptr;
     if (c->profiling) {
@@ -203,17 +200,30 @@ void launch(es_ctx* c, const char* name, double bytes, void (*kern)(KArgs...), d
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = c->st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (cluster > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)cluster;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
     CK(cudaLaunchKernelEx(&cfg, kern, args...));
     c->launches++;
     if (c->profiling) {
         CK(cudaEventRecord(ev1, c->st));
         c->prof_pending.push_back(ProfRec{name, bytes, ev0, ev1});
     }
+}
+
+template <typename... KArgs, typename... Args>
+void launch(es_ctx* c, const char* name, double bytes, void (*kern)(KArgs...), dim3 grid, dim3 block,
+            size_t smem, Args... args) {
+    launch_cl(c, name, bytes, 1, kern, grid, block, smem, args...);
 }
 
 // Fold finished event pairs into the per-kernel totals (after a sync).
@@ -627,46 +637,31 @@ Rec finish_tc(es_ctx* c, GvBuild& b, const char* name) {
     const int cols = L.npad * (L.any_pair ? 2 : 1);
     L.tmem_cols = 32;
     while (L.tmem_cols < cols) L.tmem_cols *= 2;
-    // k-ranges: when the tiles cannot fill the SMs, cut each tile's k-blocks
-    // into ranges of about work / slots k-blocks, no more units than slots
+    // k-ranges: when the tiles fill less than half the CTA slots, each tile's
+    // k-blocks are cut into cs ranges run by a cluster of cs CTAs (a power of
+    // two up to 8), each range at least 4 k-blocks long for the op with the
+    // most, and the partials fit in a CTA's shared memory
     const int slots = c->num_sms * ctas_per_sm;
-    auto assign = [&](int q) {
-        int units = 0, ctr = 0, slot = 0;
-        for (int oi = 0; oi < L.nops; ++oi) {
-            TcOp& o = L.ops[oi];
-            const int w = o.pair ? 2 : 1;
-            o.splits = q <= 0 ? 1 : std::max(1, std::min(o.nkb, (o.nkb * w + q - 1) / q));
-            o.kbps = (o.nkb + o.splits - 1) / o.splits;
-            o.splits = (o.nkb + o.kbps - 1) / o.kbps;
-            o.unit0 = units;
-            units += o.ntiles * L.rc * o.splits;
-            o.tile0 = ctr;
-            o.slot0 = slot;
-            if (o.splits > 1) {
-                ctr += o.ntiles * L.rc;
-                slot += o.ntiles * L.rc * o.splits;
-            }
-        }
-        L.nunits = units;
-        return std::make_pair(ctr, slot);
-    };
-    // A range streams at least max(4, npad / 8) k-blocks of weights (64 KB
-    // per 16 activation rows), so the partial it stores for the tile's last
-    // unit to add up (npad x 128 floats per accumulator) is at most a
-    // quarter of the weight bytes it read.
-    std::pair<int, int> used = assign(0);
-    if (tiles_all < slots) {
-        const int kb_min = std::max(4, L.npad / 8);
-        int q = std::max(kb_min, (int)std::ceil(work / slots));
-        used = assign(q);
-        const size_t slot_floats = (size_t)(L.any_pair ? 2 : 1) * L.npad * TC_BM;
-        while (L.nunits > slots || used.first > TC_COUNTERS ||
-               (size_t)used.second * slot_floats > c->tc_scratch_floats) {
-            ++q;
-            used = assign(q);
-        }
+    int nkb_max = 0;
+    for (int oi = 0; oi < L.nops; ++oi) nkb_max = std::max(nkb_max, L.ops[oi].nkb);
+    L.cs = 1;
+    if (2 * tiles_all <= slots) {
+        const int want = std::min(TC_MAX_CLUSTER, slots / tiles_all);
+        while (L.cs * 2 <= want) L.cs *= 2;
+        while (L.cs > 1 && nkb_max / L.cs < 4) L.cs /= 2;
+        const size_t red_bytes = (size_t)(L.any_pair ? 2 : 1) * L.npad * TC_BM * 4;
+        if (red_bytes > (size_t)L.stages * L.stage_bytes) L.cs = 1;
     }
-    r.grid = L.nunits;
+    int cl = 0;
+    for (int oi = 0; oi < L.nops; ++oi) {
+        TcOp& o = L.ops[oi];
+        o.kbps = (o.nkb + L.cs - 1) / L.cs;
+        o.cl0 = cl;
+        cl += o.ntiles * L.rc;
+    }
+    L.nclusters = cl;
+    r.grid = L.nclusters * L.cs;
+    r.cluster = L.cs;
     r.smem = L.stages * L.stage_bytes + 1024;
     r.bytes = wbytes + xbytes + ybytes;
     r.tc_host = T;
@@ -938,8 +933,8 @@ void run_rec(es_ctx* c, const Rec& r) {
             break;
         case R_TC:
             launch(c, "split_planes", 0.0, split_planes_kernel, dim3(r.split_grid), dim3(256), (size_t)0, r.split);
-            launch(c, r.name, r.bytes, tc_gemm_kernel, dim3(r.grid), dim3(TC_THREADS), (size_t)r.smem, r.tc,
-                   c->tc_scratch, c->tc_counters, c->status + 1);
+            launch_cl(c, r.name, r.bytes, r.cluster, tc_gemm_kernel, dim3(r.grid), dim3(TC_THREADS),
+                      (size_t)r.smem, r.tc, c->status + 1);
             break;
         case R_NORM:
             launch(c, r.name, 0.0, norm_kernel<T>, dim3(r.M), dim3(256), (size_t)0, r.norm);
@@ -1452,9 +1447,6 @@ es_status easyspec_init(const es_config* cfg, const es_weights* draft, const es_
             }
             c->tc_x_elems = 2 * rows * per_row + (size_t)128 * 2 * TC_MAX_SRCS;
             c->tc_x = c->dalloc<bf16>(c->tc_x_elems);
-            c->tc_scratch_floats = (size_t)c->num_sms * 2 * 2 * TC_BM * TC_MAXN;
-            c->tc_scratch = c->dalloc<float>(c->tc_scratch_floats);
-            c->tc_counters = c->dalloc<int>(TC_COUNTERS);
             CK(cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM_ONE));
             tensor_map_encoder();
         }

@@ -27,19 +27,24 @@
 // to its "empty" barrier, and afterwards all 8 warps read the accumulator
 // (warp w: lanes 32*(w%4).., column half w/4) and run the epilogue.
 //
-// Work split.  A unit is (op, 128-row weight tile, row chunk, range of
-// 64-column k-blocks).  When the tiles alone cannot fill the SMs, each tile's
-// k-blocks are cut into equal ranges; every range stores its partial
-// accumulator in `scratch`, and the last unit of the tile to arrive (an
-// arrival counter, no waiting) adds the partials in range order -- the
-// result does not depend on which unit arrives last -- applies the epilogue
-// and resets the counter.
+// Work split.  A unit is (op, 128-row weight tile, row chunk, k-range).  When
+// the tiles alone cannot fill the SMs, every tile's 64-column k-blocks are
+// cut into `cs` equal ranges, and the cs CTAs of one tile form a thread-block
+// cluster.  After the main loop each CTA copies its accumulator to its own
+// shared memory; after a cluster barrier, CTA s of the cluster adds the cs
+// partials of its share of the tile's columns, reading them from the other
+// CTAs' shared memory (distributed shared memory), in rank order -- the
+// result does not depend on timing -- and applies the epilogue.  A second
+// cluster barrier keeps every CTA's partial alive until all have been read.
+// Cluster CTAs are scheduled together, so the barriers need no spin loop.
 //
 // Every wait on an mbarrier is bounded (TC_WAIT_NS of the global timer).  A
 // wait that runs out sets bit 0 of `err`, the CTA stops issuing work, waits
 // (bounded again) for the copies it still has in flight, frees its tensor
 // memory and returns; the host reports ES_ERR_TIMEOUT.
 #pragma once
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "gemv.cuh"
 
@@ -52,7 +57,7 @@ constexpr int TC_THREADS = 256;
 constexpr int TC_MAX_OPS = 32;
 constexpr int TC_MAX_SEGS = 64;
 constexpr int TC_MAX_SRCS = 16;
-constexpr int TC_COUNTERS = 16384;    // arrival counters of split tiles
+constexpr int TC_MAX_CLUSTER = 8;     // k-ranges per tile (portable cluster size)
 constexpr unsigned long long TC_WAIT_NS = 2000000000ull;  // 2 s
 
 // A CUtensorMap (128 bytes, 64-byte aligned), filled on the host.
@@ -69,17 +74,15 @@ struct TcOp {
     float* y; const float* add;
     int N, ldy, epi, pair;     // pair: SwiGLU, segment seg0 = gate, seg0+1 = up
     int seg0, nseg, nkb;       // k-blocks over all segments (pair: of one)
-    int ntiles, splits, kbps;  // tiles, k-ranges per tile, k-blocks per range
-    int unit0;                 // first unit of this op
-    int tile0;                 // first arrival counter of this op's tiles
-    int slot0;                 // first partial slot (split ops)
-    int pad_;
+    int ntiles, kbps;          // tiles, k-blocks per range
+    int cl0;                   // first cluster (tile x row chunk) of this op
+    int pad_[3];
 };
 struct TcLaunch {
     TcMap maps[TC_MAX_SEGS + TC_MAX_SRCS];  // weights, then activation planes
     TcSeg segs[TC_MAX_SEGS];
     TcOp ops[TC_MAX_OPS];
-    int nops, nunits, M, rc, npad, stages, stage_bytes, tmem_cols, any_pair, pad_[7];
+    int nops, nclusters, cs, M, rc, npad, stages, stage_bytes, tmem_cols, any_pair, pad_[6];
 };
 static_assert(sizeof(TcLaunch) % 64 == 0, "descriptor keeps its maps 64-byte aligned");
 
@@ -195,17 +198,15 @@ ES_DEV void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
 }
-// 8 consecutive accumulator columns of this thread's lane.
-ES_DEV void tmem_ld8(uint32_t taddr, float* v) {
-    uint32_t r[8];
+// 8 consecutive accumulator columns of this thread's lane, issued without
+// waiting: the registers are valid after tmem_wait().
+ES_DEV void tmem_ld8(uint32_t taddr, uint32_t* r) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
                    "=r"(r[7])
                  : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
+ES_DEV void tmem_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 ES_DEV float tc_epi(int epi, float a, float b, const float* yp, const float* ap) {
     switch (epi) {
@@ -218,29 +219,28 @@ ES_DEV float tc_epi(int epi, float a, float b, const float* yp, const float* ap)
 
 // ------------------------------------------------------------ the kernel
 __global__ void __launch_bounds__(TC_THREADS, 1)
-tc_gemm_kernel(const TcLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __restrict__ counters,
-               int* __restrict__ err) {
+tc_gemm_kernel(const TcLaunch* __restrict__ Lg, int* __restrict__ err) {
     extern __shared__ __align__(1024) unsigned char tsm_raw[];
     __shared__ __align__(8) unsigned long long bars[2 * 8 + 1];
     __shared__ uint32_t s_tmem;
-    __shared__ int s_abort, s_last;
+    __shared__ int s_abort;
+    namespace cg = cooperative_groups;
     // the dynamic region is aligned to 1024 bytes by hand
     unsigned char* tsm = tsm_raw + ((1024 - (smem_u32(tsm_raw) & 1023)) & 1023);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const TcLaunch& L = *Lg;
-    const int S = L.stages, npad = L.npad;
-    // ---- which unit
-    const int unit = blockIdx.x;
+    const int S = L.stages, npad = L.npad, cs = L.cs;
+    // ---- which unit: cluster = (op, tile, row chunk), rank in it = k-range
+    const int cl = blockIdx.x / cs, split = blockIdx.x % cs;
     int oi = 0;
-    while (oi + 1 < L.nops && L.ops[oi + 1].unit0 <= unit) ++oi;
+    while (oi + 1 < L.nops && L.ops[oi + 1].cl0 <= cl) ++oi;
     const TcOp& op = L.ops[oi];
-    const int u = unit - op.unit0;
-    const int split = u % op.splits, tc = u / op.splits;
+    const int tc = cl - op.cl0;
     const int chunk = tc % L.rc, tile = tc / L.rc;
     const int kb_begin = split * op.kbps, kb_end = min(op.nkb, kb_begin + op.kbps);
-    const int nkb = kb_end - kb_begin;
-    const int pair = op.pair;
+    const int nkb = max(0, kb_end - kb_begin);
+    const int pair = op.pair, nacc = pair ? 2 : 1;
     const uint32_t w_bytes = TC_BM * TC_BK * 2;
     const uint32_t x_bytes = 2u * npad * TC_BK * 2;   // both planes
     const uint32_t tx_bytes = w_bytes * (pair ? 2 : 1) + x_bytes;
@@ -349,101 +349,118 @@ tc_gemm_kernel(const TcLaunch* __restrict__ Lg, float* __restrict__ scratch, int
     grid_dep_launch();
 
     // ---- epilogue: all warps.  The accumulator barrier completes once every
-    // MMA issued has finished (also after an abort), so the tensor memory is
-    // not freed under a running MMA.
+    // MMA issued has finished (also after an abort), so neither the tensor
+    // memory nor the stage buffers are reused under a running MMA.
     bool ok = mbar_wait(acc_bar, 0, err, abort, false);
-    ok = __all_sync(0xffffffffu, ok) && nkb > 0;
+    ok = __all_sync(0xffffffffu, ok);
     __syncthreads();
-    ok = ok && !*abort;
+    ok = ok && !*abort;            // uniform over the CTA
+    const bool have = ok && nkb > 0;  // this CTA's accumulator holds its k-range
     tc_fence_after();
     const int lq = warp & 3, half = warp >> 2;
     const int nl = lq * 32 + lane;              // accumulator lane = weight row in the tile
-    const int n = tile * TC_BM + nl;
     const int cw = npad / 2;                    // columns per warp half (multiple of 8)
     const uint32_t tl = tmem + ((uint32_t)(lq * 32) << 16);
     const int r0 = chunk * npad;
-    if (ok) {
-        if (op.splits == 1) {
-            for (int c = half * cw; c < half * cw + cw; c += 8) {
-                float a[8], b[8];
-                tmem_ld8(tl + c, a);
-                if (pair) tmem_ld8(tl + npad + c, b);
+    const int nbase = tile * TC_BM;
+    auto store = [&](int r, int n, float a, float b) {
+        float* yp = op.y + (size_t)r * op.ldy + n;
+        *yp = tc_epi(op.epi, a, b, yp, op.add ? op.add + (size_t)r * op.ldy + n : nullptr);
+    };
+    if (cs == 1) {
+        // accumulator -> registers -> y: 16 columns (and the up projection's
+        // 16) requested before one wait; for residual epilogues y is read
+        // while the tensor-memory loads are in flight
+        const int n = nbase + nl;
+        if (have) {
+            for (int c = half * cw; c < half * cw + cw; c += 16) {
+                const int nc = min(16, half * cw + cw - c);  // 16 or 8
+                uint32_t ra[16], rb[16];
+                float yv[16];
+                const bool rmw = op.epi == GEPI_ACC || op.epi == GEPI_ACC_ADD;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int r = r0 + c + i;
+                    yv[i] = 0.f;
+                    if (rmw && i < nc && r < L.M && n < op.N) {
+                        yv[i] = __ldcg(op.y + (size_t)r * op.ldy + n);
+                        if (op.epi == GEPI_ACC_ADD) yv[i] += __ldcg(op.add + (size_t)r * op.ldy + n);
+                    }
+                }
+                tmem_ld8(tl + c, ra);
+                if (nc == 16) tmem_ld8(tl + c + 8, ra + 8);
+                if (pair) {
+                    tmem_ld8(tl + npad + c, rb);
+                    if (nc == 16) tmem_ld8(tl + npad + c + 8, rb + 8);
+                }
+                tmem_wait();
                 if (n < op.N) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
+                    for (int i = 0; i < 16; ++i) {
                         const int r = r0 + c + i;
-                        if (r < L.M) {
-                            float* yp = op.y + (size_t)r * op.ldy + n;
-                            *yp = tc_epi(op.epi, a[i], pair ? b[i] : 0.f, yp,
-                                         op.add ? op.add + (size_t)r * op.ldy + n : nullptr);
-                        }
-                    }
-                }
-            }
-        } else {
-            // partial of this k-range: [acc][column][lane] at its slot
-            const int nacc = pair ? 2 : 1;
-            const size_t slot_floats = (size_t)nacc * npad * TC_BM;
-            const int tslot = op.slot0 + tc * op.splits;   // slot of the tile's range 0
-            float* part = scratch + (size_t)(tslot + split) * slot_floats;
-            for (int c = half * cw; c < half * cw + cw; c += 8) {
-                float a[8], b[8];
-                tmem_ld8(tl + c, a);
-                if (pair) tmem_ld8(tl + npad + c, b);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    part[(size_t)(c + i) * TC_BM + nl] = a[i];
-                    if (pair) part[(size_t)(npad + c + i) * TC_BM + nl] = b[i];
-                }
-            }
-            __syncthreads();
-            const int old = cta_arrive(counters + op.tile0 + tc);
-            if (tid == 0) s_last = old == op.splits - 1;
-            __syncthreads();
-            if (s_last) {
-                // sum the ranges' partials in range order, four features per
-                // thread and four ranges' loads in flight at a time
-                if (tid == 0) counters[op.tile0 + tc] = 0;
-                const float* p0 = scratch + (size_t)tslot * slot_floats;
-                const int n4 = npad * TC_BM / 4;
-                for (int e = tid; e < n4; e += TC_THREADS) {
-                    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-                    const float4* q0 = reinterpret_cast<const float4*>(p0) + e;
-                    const size_t sf4 = slot_floats / 4, acc1 = (size_t)npad * TC_BM / 4;
-                    auto add4 = [](float4& x, const float4& y) { x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w; };
-                    int sp = 0;
-                    for (; sp + 4 <= op.splits; sp += 4) {
-                        float4 v[4], w[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) v[i] = __ldcg(q0 + (sp + i) * sf4);
-                        if (pair) {
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) w[i] = __ldcg(q0 + (sp + i) * sf4 + acc1);
-                        }
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            add4(a, v[i]);
-                            if (pair) add4(b, w[i]);
-                        }
-                    }
-                    for (; sp < op.splits; ++sp) {
-                        add4(a, __ldcg(q0 + sp * sf4));
-                        if (pair) add4(b, __ldcg(q0 + sp * sf4 + acc1));
-                    }
-                    const int c = e / (TC_BM / 4), nl0 = (e % (TC_BM / 4)) * 4;
-                    const int r = r0 + c;
-                    if (r >= L.M) continue;
-                    const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int nn = tile * TC_BM + nl0 + i;
-                        if (nn >= op.N) break;
-                        float* yp = op.y + (size_t)r * op.ldy + nn;
-                        *yp = tc_epi(op.epi, av[i], bv[i], yp, op.add ? op.add + (size_t)r * op.ldy + nn : nullptr);
+                        if (i >= nc || r >= L.M) continue;
+                        const float a = __uint_as_float(ra[i]);
+                        float v;
+                        if (op.epi == GEPI_SWIGLU) v = silu_f(a) * __uint_as_float(rb[i]);
+                        else if (op.epi == GEPI_STORE) v = a;
+                        else v = yv[i] + a;
+                        op.y[(size_t)r * op.ldy + n] = v;
                     }
                 }
             }
         }
+    } else {
+        // split tile: partial accumulators meet in distributed shared memory
+        // (the stage buffers are free: every load was consumed by an MMA
+        // that has completed).  red[acc][column][lane], float32.
+        cg::cluster_group cluster = cg::this_cluster();
+        float* red = reinterpret_cast<float*>(tsm);
+        for (int c = half * cw; c < half * cw + cw; c += 8) {
+            uint32_t ra[8], rb[8];
+            if (have) {
+                tmem_ld8(tl + c, ra);
+                if (pair) tmem_ld8(tl + npad + c, rb);
+                tmem_wait();
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                red[(size_t)(c + i) * TC_BM + nl] = have ? __uint_as_float(ra[i]) : 0.f;
+                if (pair) red[(size_t)(npad + c + i) * TC_BM + nl] = have ? __uint_as_float(rb[i]) : 0.f;
+            }
+        }
+        cluster.sync();
+        // this CTA's share: columns [c0, c1) of the tile, 4 lanes per item
+        const int cper = (npad + cs - 1) / cs;
+        const int c0 = split * cper, c1 = min(npad, c0 + cper);
+        const int items = max(0, c1 - c0) * (TC_BM / 4);
+        for (int it = tid; it < items; it += TC_THREADS) {
+            const int c = c0 + it / (TC_BM / 4), l4 = (it % (TC_BM / 4)) * 4;
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+            float4 va[TC_MAX_CLUSTER], vb[TC_MAX_CLUSTER];
+            float* ea = red + (size_t)c * TC_BM + l4;
+            float* eb = red + (size_t)(npad + c) * TC_BM + l4;
+#pragma unroll
+            for (int q = 0; q < TC_MAX_CLUSTER; ++q) {
+                if (q < cs) {
+                    va[q] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(ea, q));
+                    if (pair) vb[q] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(eb, q));
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < TC_MAX_CLUSTER; ++q) {
+                if (q < cs) {
+                    a.x += va[q].x; a.y += va[q].y; a.z += va[q].z; a.w += va[q].w;
+                    if (pair) { b.x += vb[q].x; b.y += vb[q].y; b.z += vb[q].z; b.w += vb[q].w; }
+                }
+            }
+            const int r = r0 + c;
+            if (!ok || r >= L.M) continue;
+            const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (nbase + l4 + i < op.N) store(r, nbase + l4 + i, av[i], bv[i]);
+        }
+        cluster.sync();  // peers may still be reading this CTA's partial
     }
     tc_fence_before();
     __syncthreads();
