@@ -49,7 +49,7 @@ struct ArgError { std::string msg; es_status st; };
 struct Layer { const void *an, *wq, *wk, *wv, *wo, *mn, *wg, *wu, *wd; };
 
 // One kernel launch of a planned forward pass.
-enum RecKind { R_GV = 0, R_GEMM = 1, R_NORM = 2, R_ATTN = 3, R_TC = 4 };
+enum RecKind { R_GV = 0, R_GEMM = 1, R_NORM = 2, R_ATTN = 3, R_TC = 4, R_NPL = 5 };
 struct Rec {
     int kind = R_GV;
     const char* name = "";
@@ -59,7 +59,8 @@ struct Rec {
     std::shared_ptr<TcLaunch> tc_host;      // many-row bf16 pass: tensor-core descriptor on the host
     const TcLaunch* tc = nullptr;           // its device copy
     SplitArgs split{};                      // the pass's activation planes
-    int split_grid = 0, cluster = 1;
+    int split_grid = 0, cluster = 1;        // split_grid 0: planes written by the launch before
+    NormPlanesArgs npl{};                   // normalised planes for a tensor-core pass
     bool bf16 = false;                      // weights are bf16
     int nw = 8;                             // tensor-core weight pass: warps per CTA (8 or 16)
     int grid = 0, smem = 0, M = 0, ntiles64 = 0;
@@ -533,15 +534,20 @@ void encode_map(TcMap* out, const void* base, int rank, const uint64_t* dims, co
 }
 
 // Dynamic shared memory of one CTA alone on an SM (227 KB per CTA, less
-// the kernel's 1 KB of static shared memory) and the share that still lets
-// two CTAs sit on one SM (228 KB per SM).
+// the kernel's 1 KB of static shared memory), and of each of two CTAs on
+// one SM.  The second is kept to about the footprint of the decode weight
+// passes (two CTAs with windows up to 72 KB, 164 KB of the SM's memory as
+// shared memory): a pass that needs the largest carve-out forces the SM to
+// switch configurations against its neighbours.  Measured in the CUDA graph
+// of a verify step at the Llama-3-70B widths, with the gate/up pass on this
+// kernel: 3.50 ms with two 36 KB stages per CTA against 4.37 ms with three.
 constexpr int TC_SMEM_ONE = 226 * 1024;
-constexpr int TC_SMEM_TWO = 110 * 1024;
+constexpr int TC_SMEM_TWO = 80 * 1024;
 
 // A many-row bf16 weight pass: the ops of `b` become one tensor-core launch
 // (tc_gemm_kernel) preceded by one launch that writes the hi/lo planes of
 // its activation sources.
-Rec finish_tc(es_ctx* c, GvBuild& b, const char* name) {
+Rec finish_tc(es_ctx* c, GvBuild& b, const char* name, bool planes_ready = false) {
     const GvLaunch& G = *b.L;
     auto T = std::make_shared<TcLaunch>();
     memset(T.get(), 0, sizeof(TcLaunch));
@@ -587,7 +593,7 @@ Rec finish_tc(es_ctx* c, GvBuild& b, const char* name) {
             xbytes += (double)M * x.K * 4;
         }
     }
-    r.split_grid = std::max(1, std::min(4 * c->num_sms, (sa.item0[sa.nsrc] + 255) / 256));
+    r.split_grid = planes_ready ? 0 : std::max(1, std::min(4 * c->num_sms, (sa.item0[sa.nsrc] + 255) / 256));
     // ops and segments (one weight map per segment)
     int nseg = 0;
     double work = 0;
@@ -624,10 +630,10 @@ Rec finish_tc(es_ctx* c, GvBuild& b, const char* name) {
     L.nops = G.nops;
     L.any_pair = 0;
     for (int oi = 0; oi < L.nops; ++oi) L.any_pair |= L.ops[oi].pair;
-    // stages: two CTAs per SM when three stages fit in half the shared memory
+    // stages: two CTAs per SM when two stages fit in TC_SMEM_TWO
     L.stage_bytes = TC_BM * TC_BK * 2 * (L.any_pair ? 2 : 1) + 2 * L.npad * TC_BK * 2;
     int ctas_per_sm = 1;
-    if (3 * L.stage_bytes + 1024 <= TC_SMEM_TWO) {
+    if (2 * L.stage_bytes + 1024 <= TC_SMEM_TWO) {
         ctas_per_sm = 2;
         L.stages = std::min(8, (TC_SMEM_TWO - 1024) / L.stage_bytes);
     } else {
@@ -709,6 +715,23 @@ Rec norm_rec(const NormArgs& a, int rows) {
     return r;
 }
 
+// Normalised hi/lo planes of rows r*stride + off of h (h + add written
+// back first when `add` is set) for the tensor-core pass that follows.
+Rec norm_planes_rec(Model& m, const float* add, const void* gain, bf16* dst, int rows, int stride, int off) {
+    Rec r;
+    r.kind = R_NPL; r.name = "norm_planes"; r.M = rows;
+    NormPlanesArgs& a = r.npl;
+    memset(&a, 0, sizeof a);
+    a.h = m.h; a.add = add; a.g = (const bf16*)gain; a.dst = dst; a.d = m.d; a.M = rows;
+    a.src_stride = stride; a.src_off = off; a.eps = m.eps;
+    return r;
+}
+
+// Weight bytes from which a decode-size (at most 8 rows) pass runs on the
+// tensor-core kernel.
+constexpr double TC_DECODE_PAIR_BYTES = 512e6;
+constexpr double TC_DECODE_HEAD_BYTES = 1.5e9;
+
 Rec attn_rec(es_ctx* c, Model& m, int l0, int n, int M) {
     if ((size_t)M * n * m.Hkv > (size_t)ATT_COUNTERS) arg_fail(ES_ERR_ARG, "attention launch too large");
     Rec r;
@@ -743,6 +766,11 @@ struct HeadSpec { int rows = 0, stride = 1, off = 0, ldy = 0; float* y = nullptr
 Plan build_forward(es_ctx* c, Model& m, const std::vector<std::vector<int>>& groups, int mode, int M,
                    const HeadSpec& head) {
     const bool fast = M <= GV_MAXM && head.rows <= GV_MAXM;
+    // decode-size passes that stream faster on the tensor-core kernel than
+    // on the register-fed one (measured: SwiGLU pairs of 512 MB and more,
+    // output heads of 1.5 GB and more)
+    const bool tc_pair = fast && m.esz == 2 && 2.0 * m.F * m.d * m.esz >= TC_DECODE_PAIR_BYTES;
+    const bool tc_head = fast && m.esz == 2 && (double)m.V * m.d * m.esz >= TC_DECODE_HEAD_BYTES;
     Plan P;
     // -- fused path: attach a normalisation to the launch that runs just before
     //    its consumer
@@ -850,7 +878,20 @@ Plan build_forward(es_ctx* c, Model& m, const std::vector<std::vector<int>>& gro
             const Layer& y = m.ly[l0 + j];
             const float* add = fuzzy ? m.A[j] : nullptr;  // this MLP's input is h + A_j
             bool fused = false;
-            {
+            if (tc_pair) {
+                // a pair of this size streams faster through the tensor-core
+                // pass: its normalised input goes to the pass's hi/lo planes
+                // (h + A_j written back to h first)
+                GvBuild b(M, m.esz, true);
+                const int xm = b.source(m.mb[0], m.d, m.d);
+                const int o = b.op(m.F, m.s[0], m.F, GEPI_SWIGLU);
+                b.seg(o, y.wg, m.d, xm, 0);
+                b.seg(o, y.wu, m.d, xm, 1);
+                Rec t = finish_tc(c, b, label(m, "tc_gateup"), true);
+                P.recs.push_back(norm_planes_rec(m, add, y.mn, t.split.dst[0], M, 1, 0));
+                P.recs.push_back(t);
+                writer = (int)P.recs.size() - 1;
+            } else {
                 if (fast) request(add, M, 1, 0);
                 GvBuild b(M, m.esz, !fast);
                 NormArgs pre = norm_args(m, m.h, nullptr);
@@ -871,7 +912,15 @@ Plan build_forward(es_ctx* c, Model& m, const std::vector<std::vector<int>>& gro
             }
         }
     }
-    if (head.rows > 0) {
+    if (head.rows > 0 && tc_head) {
+        GvBuild b(head.rows, m.esz, true);
+        const int xs = b.source(m.xf, m.d, m.d);
+        b.seg(b.op(m.V, head.y, head.ldy, GEPI_STORE), m.lm, m.d, xs, 0);
+        Rec t = finish_tc(c, b, label(m, "tc_lm_head"), true);
+        P.recs.push_back(norm_planes_rec(m, nullptr, m.fnorm, t.split.dst[0], head.rows, head.stride, head.off));
+        P.recs.push_back(t);
+        writer = (int)P.recs.size() - 1;
+    } else if (head.rows > 0) {
         if (fast) request(nullptr, head.rows, head.stride, head.off);
         GvBuild b(head.rows, m.esz, !fast);
         NormArgs pre = norm_args(m, m.h, nullptr);
@@ -931,8 +980,13 @@ void run_rec(es_ctx* c, const Rec& r) {
             launch(c, "gemm_simt", r.bytes, gemm_kernel<T>, dim3(r.ntiles64, (r.M + GB - 1) / GB),
                    dim3(256), (size_t)0, r.gv);
             break;
+        case R_NPL:
+            launch(c, "norm_planes", 0.0, norm_planes_kernel, dim3(r.M), dim3(256), (size_t)0, r.npl);
+            break;
         case R_TC:
-            launch(c, "split_planes", 0.0, split_planes_kernel, dim3(r.split_grid), dim3(256), (size_t)0, r.split);
+            if (r.split_grid > 0)
+                launch(c, "split_planes", 0.0, split_planes_kernel, dim3(r.split_grid), dim3(256), (size_t)0,
+                       r.split);
             launch_cl(c, r.name, r.bytes, r.cluster, tc_gemm_kernel, dim3(r.grid), dim3(TC_THREADS),
                       (size_t)r.smem, r.tc, c->status + 1);
             break;

@@ -119,6 +119,42 @@ __global__ void split_planes_kernel(SplitArgs a) {
     }
 }
 
+// Normalised activation planes for a tensor-core pass that follows a
+// decode-size weight pass: one CTA per row r reads h[src] (src = r*stride +
+// off; if `add` is set, h[src] += add[src] first, written back), takes
+// rinv = 1 / sqrt(mean(h^2) + eps) and writes the hi/lo planes of
+// h * rinv * gain to dst[0][r][.], dst[1][r][.] ([2][M][d]), the values the
+// RMSNorm kernel would store in float32.
+struct NormPlanesArgs {
+    float* h; const float* add; const bf16* g; bf16* dst;
+    int d, M, src_stride, src_off;
+    float eps; int pad_;
+};
+__global__ void norm_planes_kernel(NormPlanesArgs a) {
+    __shared__ float red[32];
+    grid_dep_wait();
+    const int r = blockIdx.x;
+    const size_t src = (size_t)r * a.src_stride + a.src_off;
+    float* hr = a.h + src * a.d;
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < a.d; i += blockDim.x) {
+        float v = hr[i];
+        if (a.add) { v += a.add[src * a.d + i]; hr[i] = v; }
+        ss += v * v;
+    }
+    ss = block_sum(ss, red);
+    grid_dep_launch();
+    const float rinv = 1.0f / sqrtf(ss / (float)a.d + a.eps);
+    bf16* hi = a.dst + (size_t)r * a.d;
+    bf16* lo = hi + (size_t)a.M * a.d;
+    for (int i = threadIdx.x; i < a.d; i += blockDim.x) {
+        const float x = hr[i] * rinv * __bfloat162float(a.g[i]);
+        const bf16 h = __float2bfloat16_rn(x);
+        hi[i] = h;
+        lo[i] = __float2bfloat16_rn(x - __bfloat162float(h));
+    }
+}
+
 // ------------------------------------------------------------ PTX wrappers
 ES_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -346,7 +382,6 @@ tc_gemm_kernel(const TcLaunch* __restrict__ Lg, int* __restrict__ err) {
     }
     __syncwarp();
     grid_dep_wait();
-    grid_dep_launch();
 
     // ---- epilogue: all warps.  The accumulator barrier completes once every
     // MMA issued has finished (also after an abort), so neither the tensor
@@ -462,6 +497,10 @@ tc_gemm_kernel(const TcLaunch* __restrict__ Lg, int* __restrict__ err) {
         }
         cluster.sync();  // peers may still be reading this CTA's partial
     }
+    // dependents launch once every CTA is past its epilogue: a weight-pass
+    // CTA that started on an SM still holding this kernel's shared memory
+    // would stream through a small L1
+    grid_dep_launch();
     tc_fence_before();
     __syncthreads();
     if (warp == 1)

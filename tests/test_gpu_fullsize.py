@@ -105,3 +105,42 @@ def test_wide_window_variant_within_tolerance():
     print("wide-window bf16:", worst, rel)
     assert worst <= BF16_MAXABS and rel <= BF16_RELL2
     g.close()
+
+
+def test_tensor_core_decode_passes_at_70b_widths():
+    """At the Llama-3-70B widths (d 8192, ffn 28672, 64/8 heads) the base's
+    SwiGLU gate/up pair (940 MB) and an output head of at least 1.5 GB run
+    on the tcgen05 tensor-core kernel even at 5 rows, with the normalised
+    hi/lo planes written by the kernel before them.  One base layer and a
+    96000-token vocabulary (a 1.57 GB head) keep the float64 oracle within
+    host memory; verify logits must meet the bf16 tolerance."""
+    d = synth.shape(2, 512, 8, 2, 1376, 96000, 5e5)
+    b = synth.shape(1, 8192, 64, 8, 28672, 96000, 5e5)
+    pair = Pair(d, b, "bf16", 25)
+    gamma = 4
+    prompt = synth.make_prompts(1, 20, 96000, 26).numpy()
+    g = pair.gpu(max_seq=128, max_gamma=gamma, mode=ES_FULL_LAYER)
+    o = pair.oracle(k=1, mode=ES_FULL_LAYER, max_len=128)
+    o.block = True
+    g.easyspec_prefill(prompt)
+    o.prefill(prompt.tolist())
+    worst, rel = 0.0, 0.0
+    for ph in range(2):
+        d_gpu = g.draft_step(1, gamma, 0.0, 51 + ph)
+        o.draft_row(0, gamma, 0.0, 51 + ph, force_d=d_gpu[0])
+        n, toks = g.verify_step(0.0, 51 + ph, gamma)
+        a = int(n[0])
+        o.verify_row(0, gamma, 0.0, 51 + ph, force=(a, toks[0, : a + 1]))
+        zp = g.es_read_dist(3, gamma)[0]
+        zp_or = np.asarray(o.rows[0].zp, np.float64)
+        worst = max(worst, float(np.max(np.abs(zp - zp_or))))
+        rel = max(rel, rel_l2(zp, zp_or))
+    g.es_profile(1)
+    g.draft_step(1, gamma, 0.0, 60)
+    g.verify_step(0.0, 60, gamma)
+    kernels = g.es_profile_read()
+    g.es_profile(0)
+    print("70B-width tensor-core decode passes, bf16:", worst, rel, sorted(kernels))
+    assert "base.tc_gateup" in kernels and "base.tc_lm_head" in kernels
+    assert worst <= BF16_MAXABS and rel <= BF16_RELL2
+    g.close()
