@@ -11,7 +11,8 @@ each draft_step / verify_step sits in a nested range "draft" / "verify"
 With --table the same phases run a second time with per-launch CUDA-event
 timing and a per-kernel table (time, launches, algorithmic bytes, GB/s) is
 printed.  --base-layers / --draft-layers truncate the models (same widths)
-to keep a capture's device footprint small.
+and --vocab cuts the vocabulary of both, to keep a capture's device
+footprint small.
 """
 from __future__ import annotations
 
@@ -36,6 +37,7 @@ def main(argv=None):
     ap.add_argument("--base-layers", type=int, default=None)
     ap.add_argument("--draft-layers", type=int, default=None)
     ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--vocab", type=int, default=None)
     ap.add_argument("--table", action="store_true")
     a = ap.parse_args(argv)
 
@@ -46,6 +48,8 @@ def main(argv=None):
         sd["n_layers"] = a.draft_layers
     if a.base_layers:
         sb["n_layers"] = a.base_layers
+    if a.vocab:
+        sd["vocab"] = sb["vocab"] = a.vocab
     seed = 1000 * wl["seed"]
     wb = synth.make_weights(sb, seed + 2, wl["dtype"], "cuda")
     wd = synth.make_weights(sd, seed + 1, wl["dtype"], "cuda")
