@@ -251,6 +251,19 @@ ES_API es_status es_accept_resample_noalloc(const float *p, const float *q, cons
 ES_API es_status es_sample(const float *w, const uint64_t *u, int B, int V,
                     int32_t *idx, void *stream);
 
+/* The bounded device-side wait of the tensor-core weight passes on its own
+ * (no counterpart in the pages: it checks the library's failure path without
+ * a GPU fault).  Those passes wait on mbarriers for their TMA copies and
+ * MMAs; every wait gives up after a time limit, sets a device flag and lets
+ * the kernel free its tensor memory and return, and the host then reports
+ * ES_ERR_TIMEOUT and poisons the context.  This call runs one such wait:
+ * thread 0 waits at most limit_ns (1 ns .. 2 s) on a barrier that a second
+ * thread arrives at after arrive_ns (< 0: never; at most 1 s).  Returns
+ * ES_ERR_TIMEOUT when the wait gave up, ES_OK when the arrival came first,
+ * ES_ERR_ARG for limits out of range.  Needs no context; synchronous on
+ * `stream`; allocates and frees one int of device memory. */
+ES_API es_status es_wait_selftest(int64_t limit_ns, int64_t arrive_ns, void *stream);
+
 /* Copy cached K and V of one layer and sequence, positions [0, n), to host
  * float32 arrays k_out, v_out [n, n_kv_heads, head_dim].  which: 0 draft,
  * 1 base. */

@@ -47,6 +47,7 @@ struct AttnArgs {
     float* part;   // [M][nl][H][nsplit][hd + 2]
     int* counters; // [M][nl][Hkv]
     const int* row_pos; const int* row_seq; const int* row_base;
+    int rps, rg, ppc;   // grouped-row kernel: rows per sequence, rows per CTA group, pages per CTA
 };
 
 // dynamic shared memory (floats): qs G*(hd+4) | ks 64*(hd+4) | vs 64*(hd+4) |

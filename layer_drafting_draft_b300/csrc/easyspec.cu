@@ -23,6 +23,7 @@
 #include "../../include/easyspec.h"
 #include "kernels.cuh"
 #include "tcgemm.cuh"
+#include "attn_tc.cuh"
 
 using namespace es;
 
@@ -60,6 +61,7 @@ struct Rec {
     const TcLaunch* tc = nullptr;           // its device copy
     SplitArgs split{};                      // the pass's activation planes
     int split_grid = 0, cluster = 1;        // split_grid 0: planes written by the launch before
+    int attn_tc = 0;                        // attention: head size of the grouped-row kernel, or 0
     NormPlanesArgs npl{};                   // normalised planes for a tensor-core pass
     bool bf16 = false;                      // weights are bf16
     int nw = 8;                             // tensor-core weight pass: warps per CTA (8 or 16)
@@ -161,7 +163,7 @@ struct es_ctx {
     std::map<std::string, ProfAgg> prof;
 
     // planned forwards: key (model 0 draft / 1 base, set key, rows)
-    std::map<std::tuple<int, int, int, int, int, int>, Plan> plans;
+    std::map<std::tuple<int, int, int, int, int, int, int>, Plan> plans;
     std::map<std::tuple<int, int, int, int>, Graph> graphs;  // (part, gamma, k, B)
 
     template <typename T>
@@ -732,7 +734,13 @@ Rec norm_planes_rec(Model& m, const float* add, const void* gain, bf16* dst, int
 constexpr double TC_DECODE_PAIR_BYTES = 512e6;
 constexpr double TC_DECODE_HEAD_BYTES = 1.5e9;
 
-Rec attn_rec(es_ctx* c, Model& m, int l0, int n, int M) {
+// Attention of the layers l0 .. l0+n-1 over M rows, `rps` consecutive rows
+// per sequence.  bf16 caches with head size 64 or 128 and several rows per
+// sequence take the grouped-row tensor-core kernel when it has at least 64
+// (group, kv head, page) items: with fewer (one short sequence, few kv
+// heads) the one-row kernel's wider grid is faster (measured: the
+// Qwen2.5-0.5B/7B-shaped pair at batch 1, 2 and 4 kv heads over 5-6 pages).
+Rec attn_rec(es_ctx* c, Model& m, int l0, int n, int M, int rps) {
     if ((size_t)M * n * m.Hkv > (size_t)ATT_COUNTERS) arg_fail(ES_ERR_ARG, "attention launch too large");
     Rec r;
     r.kind = R_ATTN; r.name = "attention";
@@ -748,8 +756,22 @@ Rec attn_rec(es_ctx* c, Model& m, int l0, int n, int M) {
     r.g3 = dim3(M, n * m.Hkv, m.nsplit);
     r.bf16 = m.dtype == ES_DTYPE_BF16;
     r.smem = (int)attn_smem_bytes(m.H / m.Hkv, m.hd, m.nsplit);
-    if (r.smem > 200 * 1024) arg_fail(ES_ERR_ARG, "attention needs %d bytes of shared memory (max_seq too large)", r.smem);
     r.M = M;
+    const int G = m.H / m.Hkv;
+    const int rg = std::max(1, ATC_QV / G);
+    const int groups = rps >= 1 && M % rps == 0 ? (M / rps) * ((rps + rg - 1) / rg) * n * m.Hkv : 0;
+    if (r.bf16 && rps >= 2 && M % rps == 0 && (m.hd == 64 || m.hd == 128) && groups * m.nsplit >= 64) {
+        a.rps = rps;
+        a.rg = rg;
+        // pages per CTA: about four CTAs per SM over the cache's pages, and at
+        // most 256 chunks (the merge kernel's weight buffer)
+        a.ppc = std::max(1, std::min(m.nsplit, groups * m.nsplit / (4 * c->num_sms)));
+        a.ppc = std::max(a.ppc, (m.nsplit + 255) / 256);
+        r.attn_tc = m.hd;
+        r.g3 = dim3((M / rps) * ((rps + a.rg - 1) / a.rg), n * m.Hkv, (m.nsplit + a.ppc - 1) / a.ppc);
+        r.smem = (int)attn_tc_smem_bytes(m.hd);
+    }
+    if (r.smem > 200 * 1024) arg_fail(ES_ERR_ARG, "attention needs %d bytes of shared memory (max_seq too large)", r.smem);
     return r;
 }
 
@@ -763,7 +785,7 @@ struct HeadSpec { int rows = 0, stride = 1, off = 0, ldy = 0; float* y = nullptr
 // launch's normalised inputs are produced by the launch before it (the
 // embedding kernel for the first), RoPE and the KV append happen inside
 // attention.  Larger M: explicit norm launches and the SIMT GEMM.
-Plan build_forward(es_ctx* c, Model& m, const std::vector<std::vector<int>>& groups, int mode, int M,
+Plan build_forward(es_ctx* c, Model& m, const std::vector<std::vector<int>>& groups, int mode, int M, int rps,
                    const HeadSpec& head) {
     const bool fast = M <= GV_MAXM && head.rows <= GV_MAXM;
     // decode-size passes that stream faster on the tensor-core kernel than
@@ -849,7 +871,7 @@ Plan build_forward(es_ctx* c, Model& m, const std::vector<std::vector<int>>& gro
             if (pre.njobs) P.recs.push_back(norm_rec(pre, M));
             push_gv(b, full ? "gv_qkv_gateup" : "gv_qkv");
         }
-        P.recs.push_back(attn_rec(c, m, l0, n, M));
+        P.recs.push_back(attn_rec(c, m, l0, n, M, rps));
         P.recs.back().name = label(m, "attention");
         if (full) {
             // K-concatenated [Wo_1 .. Wo_n, Wdown_1 .. Wdown_n] . [a_1..a_n, s_1..s_n]
@@ -994,7 +1016,18 @@ void run_rec(es_ctx* c, const Rec& r) {
             launch(c, r.name, 0.0, norm_kernel<T>, dim3(r.M), dim3(256), (size_t)0, r.norm);
             break;
         default:
-            launch(c, r.name, 0.0, attn_kernel<T>, r.g3, dim3(ATT_THREADS), (size_t)r.smem, r.attn);
+            if (r.attn_tc == 64) {
+                launch(c, r.name, 0.0, attn_tc_kernel<64>, r.g3, dim3(ATC_THREADS), (size_t)r.smem, r.attn);
+                if (r.g3.z > 1)
+                    launch(c, "attention_merge", 0.0, attn_merge_kernel<64>, dim3(r.g3.x, r.g3.y, ATC_QV), dim3(64),
+                           (size_t)0, r.attn);
+            } else if (r.attn_tc == 128) {
+                launch(c, r.name, 0.0, attn_tc_kernel<128>, r.g3, dim3(ATC_THREADS), (size_t)r.smem, r.attn);
+                if (r.g3.z > 1)
+                    launch(c, "attention_merge", 0.0, attn_merge_kernel<128>, dim3(r.g3.x, r.g3.y, ATC_QV),
+                           dim3(128), (size_t)0, r.attn);
+            } else
+                launch(c, r.name, 0.0, attn_kernel<T>, r.g3, dim3(ATT_THREADS), (size_t)r.smem, r.attn);
             break;
     }
 }
@@ -1096,7 +1129,11 @@ void check_status(es_ctx* c) {
 enum { HEAD_NONE = 0, HEAD_CALIB = 1, HEAD_FUZZY = 2, HEAD_VERIFY = 3 };
 const Plan& get_forward(es_ctx* c, int key, int M, int head_kind, int step, int gamma) {
     const int which = key == -1 ? 1 : 0;
-    auto pk = std::make_tuple(which, key, M, head_kind, step, gamma);
+    // rows per sequence: one for the layer-parallel drafts, gamma+1 for
+    // calibration and verify, a chunk of positions for the prompt prefill
+    const int rps = head_kind == HEAD_FUZZY ? 1 : head_kind == HEAD_NONE ? std::max(1, M / std::max(1, c->B))
+                                                                          : gamma + 1;
+    auto pk = std::make_tuple(which, key, M, head_kind, step, gamma, rps);
     auto it = c->plans.find(pk);
     if (it != c->plans.end()) return it->second;
     std::vector<std::vector<int>> sets;
@@ -1119,7 +1156,7 @@ const Plan& get_forward(es_ctx* c, int key, int M, int head_kind, int step, int 
     if (head_kind == HEAD_CALIB) { h.rows = B; h.stride = gamma + 1; h.off = gamma; h.y = c->q_logits; h.ldy = gamma * m.V; }
     if (head_kind == HEAD_FUZZY) { h.rows = B; h.y = c->q_logits + (size_t)step * m.V; h.ldy = gamma * m.V; }
     if (head_kind == HEAD_VERIFY) { h.rows = M; h.y = c->p_logits; h.ldy = m.V; }
-    return c->plans[pk] = build_forward(c, m, sets, c->cfg.parallel_mode, M, h);
+    return c->plans[pk] = build_forward(c, m, sets, c->cfg.parallel_mode, M, rps, h);
 }
 
 // ------------------------------------------------------------------ phase parts
@@ -1525,6 +1562,8 @@ es_status easyspec_init(const es_config* cfg, const es_weights* draft, const es_
         const int att_smem = 200 * 1024;
         CK(cudaFuncSetAttribute(attn_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, att_smem));
         CK(cudaFuncSetAttribute(attn_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, att_smem));
+        CK(cudaFuncSetAttribute(attn_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
+        CK(cudaFuncSetAttribute(attn_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
         CK(cudaMallocHost(&c->h_prm, sizeof(RunParams)));
         CK(cudaMallocHost(&c->h_small, sizeof(int) * (64 + 64 * 17 + 64)));
         CK(cudaDeviceSynchronize());
@@ -1755,6 +1794,28 @@ es_status es_accept_resample_noalloc(const float* p, const float* q, const int32
     accept_kernel<<<dim3(B, a.nb), SM_THREADS, 0, st>>>(a);
     if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess) return ES_ERR_CUDA;
     return ES_OK;
+}
+
+es_status es_wait_selftest(int64_t limit_ns, int64_t arrive_ns, void* stream) {
+    if (limit_ns <= 0 || limit_ns > 2000000000ll || arrive_ns > 1000000000ll) return ES_ERR_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    int* flag = nullptr;
+    if (cudaMalloc(&flag, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return ES_ERR_OOM;
+    }
+    es_status rc = ES_OK;
+    int h = 0;
+    if (cudaMemsetAsync(flag, 0, sizeof(int), st) != cudaSuccess) rc = ES_ERR_CUDA;
+    if (rc == ES_OK) {
+        wait_selftest_kernel<<<1, 64, 0, st>>>((long long)limit_ns, (long long)arrive_ns, flag);
+        if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess ||
+            cudaMemcpy(&h, flag, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+            rc = ES_ERR_CUDA;
+    }
+    cudaFree(flag);
+    if (rc == ES_OK && h) rc = ES_ERR_TIMEOUT;
+    return rc;
 }
 
 es_status es_sample(const float* w, const uint64_t* u, int B, int V, int32_t* idx, void* stream) {

@@ -180,20 +180,45 @@ ES_DEV bool mbar_test(uint32_t bar, uint32_t parity) {
 // Wait for the phase of `parity` to complete, at most TC_WAIT_NS; false
 // (and bit 0 of *err set) when the limit ran out, or when another thread of
 // the CTA gave up (*abort) and `stop_on_abort` is set.
-ES_DEV bool mbar_wait(uint32_t bar, uint32_t parity, int* err, volatile int* abort, bool stop_on_abort = true) {
+ES_DEV bool mbar_wait(uint32_t bar, uint32_t parity, int* err, volatile int* abort, bool stop_on_abort = true,
+                      unsigned long long limit_ns = TC_WAIT_NS) {
     if (mbar_test(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_test(bar, parity)) return true;
         if ((i & 63) == 0) {
             if (stop_on_abort && *abort) return false;
-            if (global_ns() - t0 > TC_WAIT_NS) {
+            if (global_ns() - t0 > limit_ns) {
                 atomicOr(err, 1);
                 *abort = 1;
                 return false;
             }
         }
     }
+}
+
+// The bounded wait on its own: thread 0 waits at most limit_ns for an
+// mbarrier that thread 32 arrives at after arrive_ns (never when
+// arrive_ns < 0; at most 1 s).  err[0] is set when the wait gives up.
+__global__ void wait_selftest_kernel(long long limit_ns, long long arrive_ns, int* err) {
+    __shared__ __align__(8) unsigned long long bar;
+    __shared__ int abort;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        mbar_wait(smem_u32(&bar), 0, err, &abort, false, (unsigned long long)limit_ns);
+    } else if (threadIdx.x == 32 && arrive_ns >= 0) {
+        const unsigned long long t0 = global_ns();
+        const unsigned long long d = arrive_ns < 1000000000ll ? (unsigned long long)arrive_ns : 1000000000ull;
+        while (global_ns() - t0 < d) {
+        }
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bar)) : "memory");
+    }
+    __syncthreads();
 }
 
 ES_DEV void tma_load_2d(uint32_t dst, const TcMap* map, int c0, int c1, uint32_t bar) {

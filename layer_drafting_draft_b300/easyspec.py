@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "ES_OK", -1: "ES_ERR_ARG", -2: "ES_ERR_OOM", -3: "ES_ERR_CUDA
 EXPORTED = ["easyspec_init", "easyspec_prefill", "calibrate_kv", "es_set_calibration", "draft_step", "verify_step",
             "generate", "es_decode", "es_profile", "es_profile_read", "es_accept_resample",
             "es_accept_resample_noalloc",
-            "es_sample", "es_read_kv", "es_read_dist", "es_read_tokens", "es_layer_sets", "easyspec_last_error",
+            "es_sample", "es_wait_selftest", "es_read_kv", "es_read_dist", "es_read_tokens", "es_layer_sets", "easyspec_last_error",
             "easyspec_destroy"]
 
 
@@ -86,6 +86,7 @@ def lib() -> C.CDLL:
             "es_accept_resample": ([vp, vp, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, vp, vp, vp], C.c_int),
             "es_accept_resample_noalloc": ([vp, vp, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, vp, vp, vp], C.c_int),
             "es_sample": ([vp, vp, C.c_int, C.c_int, vp, vp], C.c_int),
+            "es_wait_selftest": ([C.c_int64, C.c_int64, vp], C.c_int),
             "es_read_kv": ([ctxp, C.c_int, C.c_int, C.c_int, C.c_int, f32p, f32p], C.c_int),
             "es_read_dist": ([ctxp, C.c_int, f32p], C.c_int),
             "es_read_tokens": ([ctxp, C.c_int, i32p, C.c_int, C.POINTER(C.c_int)], C.c_int),
@@ -336,3 +337,9 @@ def es_sample(w: torch.Tensor, u: torch.Tensor):
     if st != ES_OK:
         raise EasySpecError(st, "es_sample")
     return idx
+
+
+def es_wait_selftest(limit_ns: int, arrive_ns: int) -> int:
+    """Run the tensor-core passes' bounded wait alone; returns the es_status
+    (ES_ERR_TIMEOUT when the wait gave up)."""
+    return lib().es_wait_selftest(int(limit_ns), int(arrive_ns), torch.cuda.current_stream().cuda_stream)
