@@ -718,14 +718,19 @@ Rec norm_rec(const NormArgs& a, int rows) {
 }
 
 // Normalised hi/lo planes of rows r*stride + off of h (h + add written
-// back first when `add` is set) for the tensor-core pass that follows.
-Rec norm_planes_rec(Model& m, const float* add, const void* gain, bf16* dst, int rows, int stride, int off) {
+// back first when `add` is set) for the tensor-core pass that follows; ssp
+// (or nullptr) holds ss_tiles sums of squares per source row from the pass
+// before, ss_ld apart.
+Rec norm_planes_rec(Model& m, const float* add, const void* gain, bf16* dst, int rows, int stride, int off,
+                    const float* ssp, int ss_tiles, int ss_ld) {
     Rec r;
     r.kind = R_NPL; r.name = "norm_planes"; r.M = rows;
     NormPlanesArgs& a = r.npl;
     memset(&a, 0, sizeof a);
     a.h = m.h; a.add = add; a.g = (const bf16*)gain; a.dst = dst; a.d = m.d; a.M = rows;
     a.src_stride = stride; a.src_off = off; a.eps = m.eps;
+    a.ssp = ssp; a.ss_tiles = ss_tiles; a.ss_ld = ss_ld;
+    r.g3 = dim3(rows, (m.d + NPL_COLS - 1) / NPL_COLS);
     return r;
 }
 
@@ -815,6 +820,9 @@ Plan build_forward(es_ctx* c, Model& m, const std::vector<std::vector<int>>& gro
             ss_tiles = writer < 0 ? 1 : (m.d + GVM_ROWS - 1) / GVM_ROWS;
         }
     };
+    // whether the launch before can store sums of squares for the next
+    // normalisation (a register-fed pass, or the embedding kernel)
+    auto ss_writer = [&]() { return ss_mode && (writer < 0 || P.recs[writer].host); };
     // a normalised input of the launch being built: fused into its staging
     // when it fits, else written beforehand by a norm launch (which also
     // folds `add` into h) into `buf`
@@ -910,7 +918,10 @@ Plan build_forward(es_ctx* c, Model& m, const std::vector<std::vector<int>>& gro
                 b.seg(o, y.wg, m.d, xm, 0);
                 b.seg(o, y.wu, m.d, xm, 1);
                 Rec t = finish_tc(c, b, label(m, "tc_gateup"), true);
-                P.recs.push_back(norm_planes_rec(m, add, y.mn, t.split.dst[0], M, 1, 0));
+                const bool ss = ss_writer();
+                if (ss) request(add, M, 1, 0);
+                P.recs.push_back(norm_planes_rec(m, add, y.mn, t.split.dst[0], M, 1, 0, ss ? m.ssp : nullptr,
+                                                 ss ? ss_tiles : 0, M));
                 P.recs.push_back(t);
                 writer = (int)P.recs.size() - 1;
             } else {
@@ -939,7 +950,10 @@ Plan build_forward(es_ctx* c, Model& m, const std::vector<std::vector<int>>& gro
         const int xs = b.source(m.xf, m.d, m.d);
         b.seg(b.op(m.V, head.y, head.ldy, GEPI_STORE), m.lm, m.d, xs, 0);
         Rec t = finish_tc(c, b, label(m, "tc_lm_head"), true);
-        P.recs.push_back(norm_planes_rec(m, nullptr, m.fnorm, t.split.dst[0], head.rows, head.stride, head.off));
+        const bool ss = ss_writer();
+        if (ss) request(nullptr, head.rows, head.stride, head.off);
+        P.recs.push_back(norm_planes_rec(m, nullptr, m.fnorm, t.split.dst[0], head.rows, head.stride, head.off,
+                                         ss ? m.ssp : nullptr, ss ? ss_tiles : 0, M));
         P.recs.push_back(t);
         writer = (int)P.recs.size() - 1;
     } else if (head.rows > 0) {
@@ -1003,7 +1017,7 @@ void run_rec(es_ctx* c, const Rec& r) {
                    dim3(256), (size_t)0, r.gv);
             break;
         case R_NPL:
-            launch(c, "norm_planes", 0.0, norm_planes_kernel, dim3(r.M), dim3(256), (size_t)0, r.npl);
+            launch(c, "norm_planes", 0.0, norm_planes_kernel, r.g3, dim3(256), (size_t)0, r.npl);
             break;
         case R_TC:
             if (r.split_grid > 0)

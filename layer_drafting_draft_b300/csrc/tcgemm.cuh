@@ -120,38 +120,64 @@ __global__ void split_planes_kernel(SplitArgs a) {
 }
 
 // Normalised activation planes for a tensor-core pass that follows a
-// decode-size weight pass: one CTA per row r reads h[src] (src = r*stride +
-// off; if `add` is set, h[src] += add[src] first, written back), takes
+// decode-size weight pass: row r reads h[src] (src = r*stride + off; if `add`
+// is set, h[src] += add[src] first, written back), takes
 // rinv = 1 / sqrt(mean(h^2) + eps) and writes the hi/lo planes of
 // h * rinv * gain to dst[0][r][.], dst[1][r][.] ([2][M][d]), the values the
-// RMSNorm kernel would store in float32.
+// RMSNorm kernel would store in float32.  Grid (rows, column chunks of
+// NPL_COLS): the mean comes from the producing pass's per-tile sums of
+// squares (ss_tiles partials of the source row at ssp[t * ss_ld + src],
+// added by one warp lane-strided and then in a fixed shuffle order, so every
+// chunk of a row gets the same value), or, without them, from the row
+// itself.
+constexpr int NPL_COLS = 1024;
 struct NormPlanesArgs {
     float* h; const float* add; const bf16* g; bf16* dst;
+    const float* ssp; int ss_tiles, ss_ld;
     int d, M, src_stride, src_off;
-    float eps; int pad_;
+    float eps;
 };
 __global__ void norm_planes_kernel(NormPlanesArgs a) {
     __shared__ float red[32];
+    __shared__ float s_rinv;
     grid_dep_wait();
-    const int r = blockIdx.x;
+    const int r = blockIdx.x, tid = threadIdx.x;
     const size_t src = (size_t)r * a.src_stride + a.src_off;
     float* hr = a.h + src * a.d;
-    float ss = 0.f;
-    for (int i = threadIdx.x; i < a.d; i += blockDim.x) {
-        float v = hr[i];
-        if (a.add) { v += a.add[src * a.d + i]; hr[i] = v; }
-        ss += v * v;
+    const int c0 = blockIdx.y * NPL_COLS, c1 = min(a.d, c0 + NPL_COLS);
+    if (a.ssp) {
+        if (tid < 32) {
+            float t = 0.f;
+            for (int i = tid; i < a.ss_tiles; i += 32) t += __ldcg(a.ssp + (size_t)i * a.ss_ld + src);
+            t = warp_sum(t);
+            if (tid == 0) s_rinv = 1.0f / sqrtf(t / (float)a.d + a.eps);
+        }
+        __syncthreads();
+    } else {
+        float ss = 0.f;
+        for (int i = tid; i < a.d; i += blockDim.x) {
+            float v = hr[i];
+            if (a.add) v += a.add[src * a.d + i];
+            ss += v * v;
+        }
+        ss = block_sum(ss, red);
+        if (tid == 0) s_rinv = 1.0f / sqrtf(ss / (float)a.d + a.eps);
+        __syncthreads();
     }
-    ss = block_sum(ss, red);
     grid_dep_launch();
-    const float rinv = 1.0f / sqrtf(ss / (float)a.d + a.eps);
+    const float rinv = s_rinv;
     bf16* hi = a.dst + (size_t)r * a.d;
     bf16* lo = hi + (size_t)a.M * a.d;
-    for (int i = threadIdx.x; i < a.d; i += blockDim.x) {
-        const float x = hr[i] * rinv * __bfloat162float(a.g[i]);
-        const bf16 h = __float2bfloat16_rn(x);
-        hi[i] = h;
-        lo[i] = __float2bfloat16_rn(x - __bfloat162float(h));
+    for (int i = c0 + tid; i < c1; i += blockDim.x) {
+        float v = hr[i];
+        if (a.add) {
+            v += a.add[src * a.d + i];
+            hr[i] = v;
+        }
+        const float x = v * rinv * __bfloat162float(a.g[i]);
+        const bf16 hb = __float2bfloat16_rn(x);
+        hi[i] = hb;
+        lo[i] = __float2bfloat16_rn(x - __bfloat162float(hb));
     }
 }
 
