@@ -12,7 +12,8 @@ temperature 1.0), random-initialised weights and uniform prompt ids.
              calibration + fuzzy drafts + verification + accept/resample)
   e2e        the same generation through the C-ABI call generate() with host
              buffers: prompt upload, both prefills, decoding and the token
-             read-back inside the timed region (host wall clock)
+             read-back inside the timed region (host wall clock); prefill_ms
+             is the prompt prefill part of it (both models)
   draft/verify  per-phase breakdown of one more generation (the library's
              part timing: CUDA events around each phase part's graph
              launch): calibration, the gamma-1 fuzzy drafts ("fuzzy": the
@@ -348,13 +349,14 @@ def run_ours(args, rank: int, world: int):
     roof_tok_s = B * tok_per_phase / phase_roof_s
 
     # ---- e2e through generate() with host buffers
-    e2e_ms = []
+    e2e_ms, prefill_ms = [], []
     out_host = None
     for s in range(max(2, min(args.steps, 5))):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        out_host, _ = g.generate(prompts, max_new, gamma, k, T, seed0 + 500 + s)
+        out_host, gst = g.generate(prompts, max_new, gamma, k, T, seed0 + 500 + s)
         e2e_ms.append((time.perf_counter() - t0) * 1e3)
+        prefill_ms.append(gst["prefill_ms"])
     e2e_value = world * B * max_new / (max_over_ranks(statistics.mean(e2e_ms), world) / 1e3)
 
     # ---- dominant kernel: per-launch event pass over one generation
@@ -377,7 +379,8 @@ def run_ours(args, rank: int, world: int):
         "config": config_of(args, wl, gamma, world),
         "e2e": {"value": round(e2e_value, 2), "unit": "tok/s",
                 "h2d_bytes_per_step": int(prompts.size * 4 + 16 + 8),
-                "d2h_bytes_per_step": int(B * max_new * 4)},
+                "d2h_bytes_per_step": int(B * max_new * 4),
+                "prefill_ms": round(statistics.mean(prefill_ms), 2)},
         "draft": {"tok_s": round(B * gamma / (draft_ms * 1e-3), 1), "ms_per_phase": round(draft_ms, 4),
                   "achieved_gbs": round(draft_gbs, 1), "roofline_frac": round(draft_gbs / peak, 4),
                   "bytes_per_phase": int(pb["draft"]),

@@ -549,7 +549,12 @@ constexpr int TC_SMEM_TWO = 80 * 1024;
 // A many-row bf16 weight pass: the ops of `b` become one tensor-core launch
 // (tc_gemm_kernel) preceded by one launch that writes the hi/lo planes of
 // its activation sources.
-Rec finish_tc(es_ctx* c, GvBuild& b, const char* name, bool planes_ready = false) {
+// Sources whose planes their producer writes directly skip the split:
+// normalised inputs made by `pre` (the RMSNorm launch right before the
+// pass), and SwiGLU outputs of an earlier tensor-core pass in `prior` (the
+// plan so far) that nothing else reads.
+Rec finish_tc(es_ctx* c, GvBuild& b, const char* name, bool planes_ready = false, NormArgs* pre = nullptr,
+              std::vector<Rec>* prior = nullptr) {
     const GvLaunch& G = *b.L;
     auto T = std::make_shared<TcLaunch>();
     memset(T.get(), 0, sizeof(TcLaunch));
@@ -562,12 +567,20 @@ Rec finish_tc(es_ctx* c, GvBuild& b, const char* name, bool planes_ready = false
     r.kind = R_TC;
     r.name = name;
     r.M = M;
-    // activation sources -> planes in tc_x, one 3-D map each: [2][M][K]
+    // activation sources -> planes in tc_x, one 3-D map each: [2][M][K].
+    // Consecutive tensor-core passes of a plan take alternate halves of the
+    // buffer, so a pass whose epilogue writes the next pass's planes never
+    // overwrites the planes it is still reading.
     SplitArgs& sa = r.split;
     memset(&sa, 0, sizeof sa);
     sa.M = M;
     int src_of_xs[GV_MAX_XS];
     for (int i = 0; i < GV_MAX_XS; ++i) src_of_xs[i] = -1;
+    int ntc = 0;
+    if (prior)
+        for (const Rec& q : *prior) ntc += q.kind == R_TC;
+    const size_t half_elems = c->tc_x_elems / 2;
+    bf16* const base = c->tc_x + (ntc % 2) * half_elems;
     size_t off = 0;
     double wbytes = 0, xbytes = 0, ybytes = 0;
     for (int si = 0; si < G.nops; ++si) {
@@ -582,11 +595,36 @@ Rec finish_tc(es_ctx* c, GvBuild& b, const char* name, bool planes_ready = false
             if (i >= TC_MAX_SRCS) arg_fail(ES_ERR_ARG, "too many activation sources in one pass");
             src_of_xs[xs] = i;
             off = (off + 127) & ~(size_t)127;  // 256-byte aligned planes
-            if (off + 2 * (size_t)M * x.K > c->tc_x_elems)
+            if (off + 2 * (size_t)M * x.K > half_elems)
                 arg_fail(ES_ERR_ARG, "internal: activation planes exceed their buffer");
-            sa.src[i] = x.src; sa.dst[i] = c->tc_x + off; sa.ld[i] = x.ld; sa.rs[i] = x.row_stride;
+            sa.src[i] = x.src; sa.dst[i] = base + off; sa.ld[i] = x.ld; sa.rs[i] = x.row_stride;
             sa.ro[i] = x.row_off; sa.K[i] = x.K;
-            sa.item0[i + 1] = sa.item0[i] + M * (x.K / 4);
+            bool ready = planes_ready;
+            const bool plain_rows = x.row_stride == 1 && x.row_off == 0 && x.ld == x.K;
+            if (!ready && pre && plain_rows && pre->out_ld == x.K && pre->d == x.K)
+                for (int j = 0; j < pre->njobs && !ready; ++j)
+                    if (pre->out[j] == x.src) {
+                        pre->planes[j] = sa.dst[i];
+                        pre->planes_M = M;
+                        ready = true;
+                    }
+            if (!ready && prior && plain_rows)
+                for (auto it = prior->rbegin(); it != prior->rend() && !ready; ++it) {
+                    if (it->kind != R_TC || !it->tc_host) continue;
+                    TcLaunch& P = *it->tc_host;
+                    bool writes = false;
+                    for (int oi = 0; oi < P.nops; ++oi) {
+                        TcOp& o = P.ops[oi];
+                        if (o.y != x.src) continue;
+                        writes = true;
+                        if (o.epi == GEPI_SWIGLU && o.ldy == x.K && o.N == x.K && P.M == M && !o.yp) {
+                            o.yp = sa.dst[i];
+                            ready = true;
+                        }
+                    }
+                    if (writes) break;  // the most recent writer decides
+                }
+            sa.item0[i + 1] = sa.item0[i] + (ready ? 0 : M * (x.K / 4));
             const uint64_t dims[3] = {(uint64_t)x.K, (uint64_t)M, 2};
             const uint64_t strides[2] = {(uint64_t)x.K * 2, (uint64_t)M * x.K * 2};
             const uint32_t box[3] = {TC_BK, (uint32_t)L.npad, 2};
@@ -595,7 +633,7 @@ Rec finish_tc(es_ctx* c, GvBuild& b, const char* name, bool planes_ready = false
             xbytes += (double)M * x.K * 4;
         }
     }
-    r.split_grid = planes_ready ? 0 : std::max(1, std::min(4 * c->num_sms, (sa.item0[sa.nsrc] + 255) / 256));
+    r.split_grid = sa.item0[sa.nsrc] == 0 ? 0 : std::max(1, std::min(4 * c->num_sms, (sa.item0[sa.nsrc] + 255) / 256));
     // ops and segments (one weight map per segment)
     int nseg = 0;
     double work = 0;
@@ -845,8 +883,13 @@ Plan build_forward(es_ctx* c, Model& m, const std::vector<std::vector<int>>& gro
         return b.source(buf, m.d, m.d);
     };
     auto push_gv = [&](GvBuild& b, const char* name) {
-        if (!fast && m.esz == 2) P.recs.push_back(finish_tc(c, b, label(m, name)));
-        else P.recs.push_back(finish_gv(c, b, label(m, name)));
+        if (!fast && m.esz == 2) {
+            NormArgs* pre = !P.recs.empty() && P.recs.back().kind == R_NORM ? &P.recs.back().norm : nullptr;
+            Rec t = finish_tc(c, b, label(m, name), false, pre, &P.recs);
+            P.recs.push_back(t);
+        } else {
+            P.recs.push_back(finish_gv(c, b, label(m, name)));
+        }
         writer = (int)P.recs.size() - 1;
     };
     auto raw = [&](GvBuild& b, const float* p, int K) { return b.source(p, K, K); };
@@ -917,7 +960,7 @@ Plan build_forward(es_ctx* c, Model& m, const std::vector<std::vector<int>>& gro
                 const int o = b.op(m.F, m.s[0], m.F, GEPI_SWIGLU);
                 b.seg(o, y.wg, m.d, xm, 0);
                 b.seg(o, y.wu, m.d, xm, 1);
-                Rec t = finish_tc(c, b, label(m, "tc_gateup"), true);
+                Rec t = finish_tc(c, b, label(m, "tc_gateup"), true, nullptr, &P.recs);
                 const bool ss = ss_writer();
                 if (ss) request(add, M, 1, 0);
                 P.recs.push_back(norm_planes_rec(m, add, y.mn, t.split.dst[0], M, 1, 0, ss ? m.ssp : nullptr,
@@ -949,7 +992,7 @@ Plan build_forward(es_ctx* c, Model& m, const std::vector<std::vector<int>>& gro
         GvBuild b(head.rows, m.esz, true);
         const int xs = b.source(m.xf, m.d, m.d);
         b.seg(b.op(m.V, head.y, head.ldy, GEPI_STORE), m.lm, m.d, xs, 0);
-        Rec t = finish_tc(c, b, label(m, "tc_lm_head"), true);
+        Rec t = finish_tc(c, b, label(m, "tc_lm_head"), true, nullptr, &P.recs);
         const bool ss = ss_writer();
         if (ss) request(nullptr, head.rows, head.stride, head.off);
         P.recs.push_back(norm_planes_rec(m, nullptr, m.fnorm, t.split.dst[0], head.rows, head.stride, head.off,
@@ -1550,7 +1593,7 @@ es_status easyspec_init(const es_config* cfg, const es_weights* draft, const es_
                 per_row = std::max({per_row, n * (size_t)(mm->qd + mm->F), 2 * n * (size_t)mm->d,
                                     (size_t)mm->F, (size_t)mm->qd, (size_t)mm->d});
             }
-            c->tc_x_elems = 2 * rows * per_row + (size_t)128 * 2 * TC_MAX_SRCS;
+            c->tc_x_elems = 2 * (2 * rows * per_row + (size_t)128 * 2 * TC_MAX_SRCS);  // two halves
             c->tc_x = c->dalloc<bf16>(c->tc_x_elems);
             CK(cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM_ONE));
             tensor_map_encoder();

@@ -165,6 +165,9 @@ __global__ void epi_hilo_kernel(float* __restrict__ y, int ldy, const float* __r
 struct NormArgs {
     float* h; const float* add; int d; float eps; int src_stride, src_off;
     int njobs; const void* g[2 * MAX_GROUP]; float* out[2 * MAX_GROUP]; int out_ld;
+    // job j with planes[j] set writes bf16 hi/lo planes [2][planes_M][d] of
+    // its rows there (the input of a tensor-core pass) instead of out[j]
+    bf16* planes[2 * MAX_GROUP]; int planes_M;
 };
 template <typename T>
 __global__ void norm_kernel(NormArgs a) {
@@ -183,6 +186,17 @@ __global__ void norm_kernel(NormArgs a) {
     const float rinv = 1.0f / sqrtf(ss / (float)a.d + a.eps);
     for (int j = 0; j < a.njobs; ++j) {
         const T* g = (const T*)a.g[j];
+        if (a.planes[j]) {
+            bf16* hi = a.planes[j] + (size_t)r * a.d;
+            bf16* lo = hi + (size_t)a.planes_M * a.d;
+            for (int i = threadIdx.x; i < a.d; i += blockDim.x) {
+                const float x = hr[i] * rinv * to_f32(g[i]);
+                const bf16 hb = __float2bfloat16_rn(x);
+                hi[i] = hb;
+                lo[i] = __float2bfloat16_rn(x - __bfloat162float(hb));
+            }
+            continue;
+        }
         float* o = a.out[j] + (size_t)r * a.out_ld;
         for (int i = threadIdx.x; i < a.d; i += blockDim.x) o[i] = hr[i] * rinv * to_f32(g[i]);
     }

@@ -72,11 +72,13 @@ struct TcSeg {
 };
 struct TcOp {
     float* y; const float* add;
+    bf16* yp;                  // STORE / SWIGLU results as hi/lo planes [2][M][N] (the
+                               // next tensor-core pass's input) instead of y, when set
     int N, ldy, epi, pair;     // pair: SwiGLU, segment seg0 = gate, seg0+1 = up
     int seg0, nseg, nkb;       // k-blocks over all segments (pair: of one)
     int ntiles, kbps;          // tiles, k-blocks per range
     int cl0;                   // first cluster (tile x row chunk) of this op
-    int pad_[3];
+    int pad_[1];
 };
 struct TcLaunch {
     TcMap maps[TC_MAX_SEGS + TC_MAX_SRCS];  // weights, then activation planes
@@ -449,9 +451,18 @@ tc_gemm_kernel(const TcLaunch* __restrict__ Lg, int* __restrict__ err) {
     const uint32_t tl = tmem + ((uint32_t)(lq * 32) << 16);
     const int r0 = chunk * npad;
     const int nbase = tile * TC_BM;
+    auto put = [&](int r, int n, float v) {
+        if (op.yp) {
+            const bf16 hb = __float2bfloat16_rn(v);
+            op.yp[(size_t)r * op.N + n] = hb;
+            op.yp[(size_t)L.M * op.N + (size_t)r * op.N + n] = __float2bfloat16_rn(v - __bfloat162float(hb));
+        } else {
+            op.y[(size_t)r * op.ldy + n] = v;
+        }
+    };
     auto store = [&](int r, int n, float a, float b) {
-        float* yp = op.y + (size_t)r * op.ldy + n;
-        *yp = tc_epi(op.epi, a, b, yp, op.add ? op.add + (size_t)r * op.ldy + n : nullptr);
+        const float* yp = op.y + (size_t)r * op.ldy + n;
+        put(r, n, tc_epi(op.epi, a, b, yp, op.add ? op.add + (size_t)r * op.ldy + n : nullptr));
     };
     if (cs == 1) {
         // accumulator -> registers -> y: 16 columns (and the up projection's
@@ -490,7 +501,7 @@ tc_gemm_kernel(const TcLaunch* __restrict__ Lg, int* __restrict__ err) {
                         if (op.epi == GEPI_SWIGLU) v = silu_f(a) * __uint_as_float(rb[i]);
                         else if (op.epi == GEPI_STORE) v = a;
                         else v = yv[i] + a;
-                        op.y[(size_t)r * op.ldy + n] = v;
+                        put(r, n, v);
                     }
                 }
             }
