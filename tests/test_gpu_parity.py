@@ -93,6 +93,11 @@ def test_tiny_f32_generate_bit_exact(tiny, T):
         from oracle import spec
         assert want[0] == spec.seq_decode(tiny.Wb, tiny.shape_b, prompt[0].tolist(), TINY["max_new"])
     assert st["emitted"] >= TINY["max_new"] and st["phases"] >= 1
+    # the run's counters: host wall-clock times of both parts, launches of
+    # this library while decoding, drafts proposed to unfinished sequences
+    assert st["prefill_ms"] > 0 and st["decode_ms"] > 0
+    assert st["kernel_launches"] >= st["phases"] > 0
+    assert st["drafted"] == TINY["gamma"] * st["phases"] and 0 <= st["accepted"] <= st["drafted"]
     g.close()
 
 
