@@ -535,16 +535,7 @@ void encode_map(TcMap* out, const void* base, int rank, const uint64_t* dims, co
     if (r != CUDA_SUCCESS) arg_fail(ES_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
 }
 
-// Dynamic shared memory of one CTA alone on an SM (227 KB per CTA, less
-// the kernel's 1 KB of static shared memory), and of each of two CTAs on
-// one SM.  The second is kept to about the footprint of the decode weight
-// passes (two CTAs with windows up to 72 KB, 164 KB of the SM's memory as
-// shared memory): a pass that needs the largest carve-out forces the SM to
-// switch configurations against its neighbours.  Measured in the CUDA graph
-// of a verify step at the Llama-3-70B widths, with the gate/up pass on this
-// kernel: 3.50 ms with two 36 KB stages per CTA against 4.37 ms with three.
-constexpr int TC_SMEM_ONE = 226 * 1024;
-constexpr int TC_SMEM_TWO = 80 * 1024;
+
 
 // A many-row bf16 weight pass: the ops of `b` become one tensor-core launch
 // (tc_gemm_kernel) preceded by one launch that writes the hi/lo planes of
@@ -561,8 +552,8 @@ Rec finish_tc(es_ctx* c, GvBuild& b, const char* name, bool planes_ready = false
     TcLaunch& L = *T;
     const int M = G.M;
     L.M = M;
-    L.rc = (M + TC_MAXN - 1) / TC_MAXN;
-    L.npad = ((M + L.rc - 1) / L.rc + 15) / 16 * 16;
+    L.rc = (M + TC_MAXN - 1) / TC_MAXN;                       // as tc_layout sets them:
+    L.npad = ((M + L.rc - 1) / L.rc + 15) / 16 * 16;          // the activation maps' box needs npad
     Rec r;
     r.kind = R_TC;
     r.name = name;
@@ -636,8 +627,6 @@ Rec finish_tc(es_ctx* c, GvBuild& b, const char* name, bool planes_ready = false
     r.split_grid = sa.item0[sa.nsrc] == 0 ? 0 : std::max(1, std::min(4 * c->num_sms, (sa.item0[sa.nsrc] + 255) / 256));
     // ops and segments (one weight map per segment)
     int nseg = 0;
-    double work = 0;
-    int tiles_all = 0;
     for (int oi = 0; oi < G.nops; ++oi) {
         const GvOp& go = G.ops[oi];
         TcOp& o = L.ops[oi];
@@ -662,50 +651,11 @@ Rec finish_tc(es_ctx* c, GvBuild& b, const char* name, bool planes_ready = false
             wbytes += (double)go.N * g.K * 2;
             ++nseg;
         }
-        o.ntiles = (go.N + TC_BM - 1) / TC_BM;
-        tiles_all += o.ntiles * L.rc;
-        work += (double)o.ntiles * L.rc * o.nkb * (o.pair ? 2 : 1);
         ybytes += (double)M * go.N * 4 * (go.epi == GEPI_ACC ? 2 : go.epi == GEPI_ACC_ADD ? 3 : 1);
     }
     L.nops = G.nops;
-    L.any_pair = 0;
-    for (int oi = 0; oi < L.nops; ++oi) L.any_pair |= L.ops[oi].pair;
-    // stages: two CTAs per SM when two stages fit in TC_SMEM_TWO
-    L.stage_bytes = TC_BM * TC_BK * 2 * (L.any_pair ? 2 : 1) + 2 * L.npad * TC_BK * 2;
-    int ctas_per_sm = 1;
-    if (2 * L.stage_bytes + 1024 <= TC_SMEM_TWO) {
-        ctas_per_sm = 2;
-        L.stages = std::min(8, (TC_SMEM_TWO - 1024) / L.stage_bytes);
-    } else {
-        L.stages = std::min(8, (TC_SMEM_ONE - 1024) / L.stage_bytes);
-    }
-    if (L.stages < 2) arg_fail(ES_ERR_ARG, "internal: tensor-core stage of %d bytes too large", L.stage_bytes);
-    const int cols = L.npad * (L.any_pair ? 2 : 1);
-    L.tmem_cols = 32;
-    while (L.tmem_cols < cols) L.tmem_cols *= 2;
-    // k-ranges: when the tiles fill less than half the CTA slots, each tile's
-    // k-blocks are cut into cs ranges run by a cluster of cs CTAs (a power of
-    // two up to 8), each range at least 4 k-blocks long for the op with the
-    // most, and the partials fit in a CTA's shared memory
-    const int slots = c->num_sms * ctas_per_sm;
-    int nkb_max = 0;
-    for (int oi = 0; oi < L.nops; ++oi) nkb_max = std::max(nkb_max, L.ops[oi].nkb);
-    L.cs = 1;
-    if (2 * tiles_all <= slots) {
-        const int want = std::min(TC_MAX_CLUSTER, slots / tiles_all);
-        while (L.cs * 2 <= want) L.cs *= 2;
-        while (L.cs > 1 && nkb_max / L.cs < 4) L.cs /= 2;
-        const size_t red_bytes = (size_t)(L.any_pair ? 2 : 1) * L.npad * TC_BM * 4;
-        if (red_bytes > (size_t)L.stages * L.stage_bytes) L.cs = 1;
-    }
-    int cl = 0;
-    for (int oi = 0; oi < L.nops; ++oi) {
-        TcOp& o = L.ops[oi];
-        o.kbps = (o.nkb + L.cs - 1) / L.cs;
-        o.cl0 = cl;
-        cl += o.ntiles * L.rc;
-    }
-    L.nclusters = cl;
+    if (tc_layout(L, c->num_sms) == 0)
+        arg_fail(ES_ERR_ARG, "internal: tensor-core stage of %d bytes too large", L.stage_bytes);
     r.grid = L.nclusters * L.cs;
     r.cluster = L.cs;
     r.smem = L.stages * L.stage_bytes + 1024;
@@ -773,8 +723,9 @@ Rec norm_planes_rec(Model& m, const float* add, const void* gain, bf16* dst, int
 }
 
 // Weight bytes from which a decode-size (at most 8 rows) pass runs on the
-// tensor-core kernel.
-constexpr double TC_DECODE_PAIR_BYTES = 512e6;
+// tensor-core kernel.  Pairs: the 7B- and 70B-shaped base gate/up (272 MB,
+// 940 MB) gain; the 8B-shaped draft's (235 MB) measured no faster.
+constexpr double TC_DECODE_PAIR_BYTES = 256e6;
 constexpr double TC_DECODE_HEAD_BYTES = 1.5e9;
 
 // Attention of the layers l0 .. l0+n-1 over M rows, `rps` consecutive rows
@@ -832,7 +783,7 @@ Plan build_forward(es_ctx* c, Model& m, const std::vector<std::vector<int>>& gro
                    const HeadSpec& head) {
     const bool fast = M <= GV_MAXM && head.rows <= GV_MAXM;
     // decode-size passes that stream faster on the tensor-core kernel than
-    // on the register-fed one (measured: SwiGLU pairs of 512 MB and more,
+    // on the register-fed one (measured: SwiGLU pairs of 256 MB and more,
     // output heads of 1.5 GB and more)
     const bool tc_pair = fast && m.esz == 2 && 2.0 * m.F * m.d * m.esz >= TC_DECODE_PAIR_BYTES;
     const bool tc_head = fast && m.esz == 2 && (double)m.V * m.d * m.esz >= TC_DECODE_HEAD_BYTES;

@@ -88,6 +88,89 @@ struct TcLaunch {
 };
 static_assert(sizeof(TcLaunch) % 64 == 0, "descriptor keeps its maps 64-byte aligned");
 
+// Dynamic shared memory of one CTA alone on an SM (227 KB per CTA, less
+// the kernel's 1 KB of static shared memory), and of each of two CTAs on
+// one SM.  The second is kept to about the footprint of the decode weight
+// passes (two CTAs with windows up to 72 KB, 164 KB of the SM's memory as
+// shared memory): a pass that needs the largest carve-out forces the SM to
+// switch configurations against its neighbours.  Measured in the CUDA graph
+// of a verify step at the Llama-3-70B widths, with the gate/up pass on this
+// kernel: 3.50 ms with two 36 KB stages per CTA against 4.37 ms with three.
+constexpr int TC_SMEM_ONE = 226 * 1024;
+constexpr int TC_SMEM_TWO = 80 * 1024;
+
+// Layout of a launch whose rows (M) and ops (N, pair, nkb per op) are set:
+// row chunks of at most TC_MAXN rows padded to a multiple of 16; stages
+// (two CTAs per SM when two stages fit in TC_SMEM_TWO, else one CTA with up
+// to 8 stages); tensor-memory columns; and, when the tiles fill less than
+// half the CTA slots, cs k-ranges per tile run by a cluster of cs CTAs (a
+// power of two up to TC_MAX_CLUSTER, each range at least 4 k-blocks long
+// for the op with the most, and the partials fit in the CTA's shared
+// memory).  Returns the CTAs per SM, or 0 when a stage does not fit twice.
+inline int tc_layout(TcLaunch& L, int num_sms) {
+    L.rc = (L.M + TC_MAXN - 1) / TC_MAXN;
+    L.npad = ((L.M + L.rc - 1) / L.rc + 15) / 16 * 16;
+    L.any_pair = 0;
+    int tiles_all = 0, nkb_max = 0;
+    for (int oi = 0; oi < L.nops; ++oi) {
+        TcOp& o = L.ops[oi];
+        L.any_pair |= o.pair;
+        o.ntiles = (o.N + TC_BM - 1) / TC_BM;
+        tiles_all += o.ntiles * L.rc;
+        nkb_max = o.nkb > nkb_max ? o.nkb : nkb_max;
+    }
+    L.stage_bytes = TC_BM * TC_BK * 2 * (L.any_pair ? 2 : 1) + 2 * L.npad * TC_BK * 2;
+    int ctas_per_sm = 1;
+    if (2 * L.stage_bytes + 1024 <= TC_SMEM_TWO) {
+        ctas_per_sm = 2;
+        L.stages = (TC_SMEM_TWO - 1024) / L.stage_bytes;
+    } else {
+        L.stages = (TC_SMEM_ONE - 1024) / L.stage_bytes;
+    }
+    L.stages = L.stages < 8 ? L.stages : 8;
+    if (L.stages < 2) return 0;
+    const int cols = L.npad * (L.any_pair ? 2 : 1);
+    L.tmem_cols = 32;
+    while (L.tmem_cols < cols) L.tmem_cols *= 2;
+    const int slots = num_sms * ctas_per_sm;
+    L.cs = 1;
+    if (2 * tiles_all <= slots) {
+        const int want = slots / tiles_all < TC_MAX_CLUSTER ? slots / tiles_all : TC_MAX_CLUSTER;
+        while (L.cs * 2 <= want) L.cs *= 2;
+        while (L.cs > 1 && nkb_max / L.cs < 4) L.cs /= 2;
+        const size_t red_bytes = (size_t)(L.any_pair ? 2 : 1) * L.npad * TC_BM * 4;
+        if (red_bytes > (size_t)L.stages * L.stage_bytes) L.cs = 1;
+    }
+    int cl = 0;
+    for (int oi = 0; oi < L.nops; ++oi) {
+        TcOp& o = L.ops[oi];
+        o.kbps = (o.nkb + L.cs - 1) / L.cs;
+        o.cl0 = cl;
+        cl += o.ntiles * L.rc;
+    }
+    L.nclusters = cl;
+    return ctas_per_sm;
+}
+
+// The work of CTA `block`: its cluster is (op, tile, row chunk); its rank in
+// the cluster is its k-range [kb_begin, kb_end) of the op's k-blocks
+// (possibly empty).
+struct TcUnit { int op, tile, chunk, split, kb_begin, kb_end; };
+__host__ __device__ inline TcUnit tc_unit(const TcLaunch& L, int block) {
+    TcUnit u;
+    const int cl = block / L.cs;
+    u.split = block % L.cs;
+    u.op = 0;
+    while (u.op + 1 < L.nops && L.ops[u.op + 1].cl0 <= cl) ++u.op;
+    const TcOp& o = L.ops[u.op];
+    const int tc = cl - o.cl0;
+    u.chunk = tc % L.rc;
+    u.tile = tc / L.rc;
+    u.kb_begin = u.split * o.kbps < o.nkb ? u.split * o.kbps : o.nkb;
+    u.kb_end = u.kb_begin + o.kbps < o.nkb ? u.kb_begin + o.kbps : o.nkb;
+    return u;
+}
+
 // Activation planes: for source i, rows r*row_stride + row_off of src
 // (leading dimension ld, K columns) become hi/lo bf16 planes
 // dst[0][r][k], dst[1][r][k] ([2][M][K]).
@@ -321,15 +404,11 @@ tc_gemm_kernel(const TcLaunch* __restrict__ Lg, int* __restrict__ err) {
     const TcLaunch& L = *Lg;
     const int S = L.stages, npad = L.npad, cs = L.cs;
     // ---- which unit: cluster = (op, tile, row chunk), rank in it = k-range
-    const int cl = blockIdx.x / cs, split = blockIdx.x % cs;
-    int oi = 0;
-    while (oi + 1 < L.nops && L.ops[oi + 1].cl0 <= cl) ++oi;
-    const TcOp& op = L.ops[oi];
-    const int tc = cl - op.cl0;
-    const int chunk = tc % L.rc, tile = tc / L.rc;
-    const int kb_begin = split * op.kbps, kb_end = min(op.nkb, kb_begin + op.kbps);
-    const int nkb = max(0, kb_end - kb_begin);
-    const int pair = op.pair, nacc = pair ? 2 : 1;
+    const TcUnit U = tc_unit(L, blockIdx.x);
+    const TcOp& op = L.ops[U.op];
+    const int split = U.split, chunk = U.chunk, tile = U.tile;
+    const int kb_begin = U.kb_begin, nkb = U.kb_end - U.kb_begin;
+    const int pair = op.pair;
     const uint32_t w_bytes = TC_BM * TC_BK * 2;
     const uint32_t x_bytes = 2u * npad * TC_BK * 2;   // both planes
     const uint32_t tx_bytes = w_bytes * (pair ? 2 : 1) + x_bytes;

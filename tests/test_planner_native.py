@@ -26,3 +26,19 @@ def test_walker_and_windows(tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stdout + r.stderr[-3000:]
     assert "0 failed checks" in r.stdout
+
+
+def test_tensor_core_pass_layout_and_units(tmp_path):
+    """tests/native/tc_plan_check.cu drives tc_layout and tc_unit (the
+    planner's and the kernel's own functions) over 3000 random launches:
+    row chunks, stages, shared memory for one or two CTAs per SM, tensor-
+    memory columns, cluster size, and that the grid's CTAs partition every
+    tile's k-blocks in rank order.  Compiled with nvcc; no GPU."""
+    exe = str(tmp_path / "tc_plan_check")
+    cmd = [build.nvcc(), *build.ARCH, "-std=c++17", "--expt-relaxed-constexpr", "-O2", "-I", CSRC,
+           "-o", exe, os.path.join(HERE, "native", "tc_plan_check.cu")]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr[-3000:]
+    assert " 0 failed checks" in r.stdout
