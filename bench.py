@@ -114,14 +114,15 @@ def measured_traffic(kernel: str, workload: str, rows: int):
         return None
     with open(path) as f:
         t = json.load(f)
-    e = t.get(kernel)
-    if not e or e.get("workload") != workload or e.get("rows") != rows:
-        return None
-    h = hashlib.sha256()
-    for rel in e["sources"]:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
-    return e["dram_bytes_per_launch"] if h.hexdigest() == e["sources_sha256"] else None
+    for e in t.get(kernel, []):
+        if e.get("workload") != workload or e.get("rows") != rows:
+            continue
+        h = hashlib.sha256()
+        for rel in e["sources"]:
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                h.update(f.read())
+        return e["dram_bytes_per_launch"] if h.hexdigest() == e["sources_sha256"] else None
+    return None
 
 
 def peaks():

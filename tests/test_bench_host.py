@@ -43,9 +43,15 @@ def test_kv_bytes_per_position():
 def test_traffic_only_for_the_captured_workload_and_rows():
     with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
         t = json.load(f)
-    e = t["base.gv_gateup"]
-    got = bench.measured_traffic("base.gv_gateup", e["workload"], e["rows"])
-    assert got in (e["dram_bytes_per_launch"], None)   # None once the kernel sources change
-    assert bench.measured_traffic("base.gv_gateup", e["workload"], e["rows"] + 1) is None
-    assert bench.measured_traffic("base.gv_gateup", "qwen2.5_longctx_bf16", e["rows"]) is None
+    for name in ("base.gv_gateup", "base.tc_gateup"):
+        for e in t[name]:
+            got = bench.measured_traffic(name, e["workload"], e["rows"])
+            assert got in (e["dram_bytes_per_launch"], None)   # None once the kernel sources change
+            assert bench.measured_traffic(name, e["workload"], e["rows"] + 1) is None
+            assert bench.measured_traffic(name, "qwen2.5_longctx_bf16", e["rows"]) is None
+    e = t["base.tc_gateup"][0]
     assert bench.measured_traffic("no.such_pass", e["workload"], e["rows"]) is None
+    # two workloads of one pass keep their own figures
+    by = {e["workload"]: e["dram_bytes_per_launch"] for e in t["base.tc_gateup"]}
+    assert bench.measured_traffic("base.tc_gateup", "llama3_8b_70b_bf16", 5) == by["llama3_8b_70b_bf16"]
+    assert bench.measured_traffic("base.tc_gateup", "qwen2.5_0.5b_7b_bf16", 5) == by["qwen2.5_0.5b_7b_bf16"]
