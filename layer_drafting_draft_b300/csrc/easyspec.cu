@@ -308,8 +308,13 @@ void setup_model(es_ctx* c, Model& m, const es_model_shape& s, const es_weights*
         }
     m.rope = c->dalloc<float>(rt.size());
     CK(cudaMemcpy(m.rope, rt.data(), rt.size() * sizeof(float), cudaMemcpyHostToDevice));
-    // workspace rows: decode batches and prefill chunks
-    m.Mw = std::max(Bmax * (c->cfg.max_gamma + 1), 256);
+    // workspace rows: decode batches and prefill chunks.  A prompt is
+    // prefilled in chunks of Mw / B positions per sequence, each a full pass
+    // over the weights: 1024 rows keep the tensor-core passes' row chunks
+    // (256 rows each) several per tile, and stream the weights a quarter as
+    // often as 256 rows did (long-context pair, batch 16, 4096-token
+    // prompts: prefill 5.8 -> 3.9 s).
+    m.Mw = std::max(Bmax * (c->cfg.max_gamma + 1), 1024);
     m.slots = slots;
     const size_t Mw = m.Mw;
     m.h = c->dalloc<float>(Mw * m.d);
