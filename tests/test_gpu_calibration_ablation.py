@@ -95,3 +95,49 @@ def test_switch_rejected_mid_phase(tiny):
     g.es_set_calibration(False)
     g.es_set_calibration(True)
     g.close()
+
+
+def test_bf16_no_calibration_grouped_row_attention():
+    """bf16 self-draft pair with 8 kv heads and 8 KV pages of capacity: the
+    calibration and verify attention run on the grouped-row tensor-core
+    kernel (at least 64 group x kv head x page items), where the narrowed
+    calibration window has inactive rows (positions with a kept fuzzy entry)
+    inside a group. Teacher-forced on the GPU's tokens, the draft and base
+    logits meet the bf16 tolerance against the oracle under the same switch,
+    and the draft cache, kept fuzzy entries included, equals the oracle's to
+    the cache's bf16 rounding."""
+    s = synth.shape(4, 512, 8, 8, 1376, 1000, 1e4)
+    pair = Pair(s, s, "bf16", 37, sigma=0.1)
+    gamma, T, seed, k = 4, 1.0, 91, 2
+    prompt = synth.make_prompts(1, 300, 1000, 38).numpy()
+    g = pair.gpu(max_seq=512, max_gamma=gamma, mode=ES_FULL_LAYER)
+    g.es_set_calibration(False)
+    o = pair.oracle(k=k, mode=ES_FULL_LAYER, max_len=512, calibrate=False)
+    o.block = True
+    g.easyspec_prefill(prompt)
+    o.prefill(prompt.tolist())
+    worst, kept = 0.0, 0
+    for ph in range(10):
+        d_gpu = g.draft_step(k, gamma, T, seed)
+        o.draft_row(0, gamma, T, seed, force_d=d_gpu[0])
+        worst = max(worst, float(np.max(np.abs(g.es_read_dist(2, gamma)[0] - o.rows[0].zq))))
+        n, toks = g.verify_step(T, seed, gamma)
+        a = int(n[0])
+        o.verify_row(0, gamma, T, seed, force=(a, toks[0, : a + 1]))
+        worst = max(worst, float(np.max(np.abs(g.es_read_dist(3, gamma)[0] - o.rows[0].zp))))
+        kept += min(a, gamma - 1)
+    assert worst <= 3e-2, worst
+    assert kept >= 2, kept        # some fuzzy entries were kept (inactive calibration rows)
+    g.es_profile(1)               # the grouped kernel's chunk merge runs: the path is the one meant
+    g.calibrate_kv(gamma, T, seed)
+    assert "attention_merge" in g.es_profile_read()
+    g.es_profile(0)
+    o.calibrate_row(o.rows[0])
+    r = o.rows[0]
+    n = len(r.tokens)
+    for layer in range(s["n_layers"]):
+        kk, vv = g.es_read_kv(0, layer, 0, n, s["n_kv_heads"], s["head_dim"])
+        scale = max(1.0, float(np.max(np.abs(r.draft.K[layer, :n]))))
+        assert np.max(np.abs(kk - r.draft.K[layer, :n])) <= 2e-2 * scale, layer
+        assert np.max(np.abs(vv - r.draft.V[layer, :n])) <= 2e-2 * max(1.0, float(np.max(np.abs(r.draft.V[layer, :n])))), layer
+    g.close()
