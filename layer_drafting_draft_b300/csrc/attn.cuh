@@ -32,12 +32,6 @@ constexpr int ATT_COUNTERS = 16384;
 struct KVGeom {
     void* kv; const int* page_table; int pages_per_seq, L, Hkv, hd, max_seq;
 };
-template <typename T>
-ES_DEV T* kv_ptr(const KVGeom& g, int seq, int pos, int layer, int kv, int h) {
-    const int page = g.page_table[seq * g.pages_per_seq + pos / PAGE];
-    const size_t off = ((((size_t)page * g.L + layer) * 2 + kv) * g.Hkv + h) * PAGE + pos % PAGE;
-    return (T*)g.kv + off * g.hd;
-}
 
 struct AttnArgs {
     KVGeom g; const float* rope; int H, M, nl, nsplit;
@@ -47,7 +41,7 @@ struct AttnArgs {
     float* part;   // [M][nl][H][nsplit][hd + 2]
     int* counters; // [M][nl][Hkv]
     const int* row_pos; const int* row_seq; const int* row_base;
-    int rps, rg, ppc;   // grouped-row kernel: rows per sequence, rows per CTA group, pages per CTA
+    int rps, rg, ppc;   // rows per sequence (0: no fixed layout); grouped-row kernel: rows per CTA group, pages per CTA
 };
 
 // dynamic shared memory (floats): qs G*(hd+4) | ks 64*(hd+4) | vs 64*(hd+4) |
@@ -56,11 +50,6 @@ inline size_t attn_smem_bytes(int G, int hd, int nsplit) {
     return sizeof(float) * ((size_t)G * (hd + 4) + 2 * 64 * (hd + 4) + (size_t)G * (nsplit > 64 ? nsplit : 64));
 }
 
-// A cache element read through L2 (entries are written by other CTAs).
-ES_DEV float ldcg_f(const float* p) { return __ldcg(p); }
-ES_DEV float ldcg_f(const bf16* p) {
-    return __uint_as_float((uint32_t)__ldcg(reinterpret_cast<const unsigned short*>(p)) << 16);
-}
 
 // One work item: row m, layer slot x kv head `jy`, position split `sp`.
 // Whole CTA (ATT_THREADS threads).
@@ -69,12 +58,20 @@ ES_DEV void attn_item(const AttnArgs& a, int m, int jy, int sp) {
     extern __shared__ __align__(16) float asm_[];
     __shared__ int s_last;
     const int Hkv = a.g.Hkv, hd = a.g.hd, half = hd / 2, G = a.H / Hkv, ld = hd + 4;
-    const int j = jy / Hkv, hk = jy % Hkv;
-    const int pos = __ldcg(a.row_pos + m);
+    const int j = jy / Hkv, hk = jy % Hkv, pps = a.g.pages_per_seq;
+    // The row's descriptors in one round of loads.  With rps rows per
+    // sequence laid out sequence by sequence the row's sequence is m / rps,
+    // which gives the split's page at the same time (looked up again below if
+    // row_seq says otherwise).
+    const int guess = a.rps > 0 ? m / a.rps : -1;
+    const int pos = __ldcg(a.row_pos + m), rb = __ldcg(a.row_base + m), seq = __ldcg(a.row_seq + m);
+    const int pg_guess = guess >= 0 && sp < pps ? __ldcg(a.g.page_table + (size_t)guess * pps + sp) : -1;
     const int p0 = sp * PAGE;
     if (pos < 0 || p0 > pos) return;
     const int n = min(PAGE, pos + 1 - p0);
-    const int rb = __ldcg(a.row_base + m), bpos = __ldcg(a.row_pos + rb), seq = __ldcg(a.row_seq + m);
+    // the rows of a block hold consecutive positions from its first row on
+    const int bpos = pos - (m - rb);
+    const int page = seq == guess ? pg_guess : a.g.page_table[(size_t)seq * pps + sp];
     const int tid = threadIdx.x, layer = a.layer[j];
     float* qs = asm_;
     float* ks = qs + G * ld;
@@ -83,14 +80,17 @@ ES_DEV void attn_item(const AttnArgs& a, int m, int jy, int sp) {
     const float scale = 1.0f / sqrtf((float)hd);
     const int kvd = Hkv * hd, qd = a.H * hd;
 
-    const bool cached = p0 + n <= bpos;  // every position of this split is in the cache
-    // Issue the independent global loads together: the cached K/V page of
-    // this split (16-byte vectors), the queries and their rotation factors.
+    // positions of this split already in the cache (all but the launch's own)
+    const int ncached = max(0, min(n, bpos - p0));
+    // Issue the independent global loads together: the cached part of the
+    // split's K/V page (16-byte vectors), the queries and their rotation
+    // factors.
     constexpr int EPV = 16 / sizeof(T);
     constexpr int VPT = 8;  // vectors of K (and of V) per thread and pass
-    const int nv = n * hd / EPV;
-    const T* Kp = kv_ptr<T>(a.g, seq, p0, layer, 0, hk);
-    const T* Vp = kv_ptr<T>(a.g, seq, p0, layer, 1, hk);
+    const int nv = ncached * hd / EPV;
+    const size_t kvoff = ((((size_t)page * a.g.L + layer) * 2) * Hkv + hk) * PAGE * hd;
+    const T* Kp = (const T*)a.g.kv + kvoff;
+    const T* Vp = Kp + (size_t)Hkv * PAGE * hd;
     const float* q = a.q[j] + (size_t)m * qd + (size_t)hk * G * hd;
     const float* csq = a.rope + (size_t)pos * hd;
     // A cached page was written by earlier launches, and the row
@@ -108,11 +108,11 @@ ES_DEV void attn_item(const AttnArgs& a, int m, int jy, int sp) {
             }
         }
     };
-    if (cached) load_pass(0);
+    if (nv > 0) load_pass(0);
     grid_dep_wait();
     grid_dep_launch();
-    for (int base = 0; base < (cached ? nv : 0) || base == 0; base += VPT * ATT_THREADS) {
-        if (cached && base > 0) load_pass(base);
+    for (int base = 0; base < nv || base == 0; base += VPT * ATT_THREADS) {
+        if (base > 0) load_pass(base);
         if (base == 0) {
             for (int t = tid; t < G * half; t += ATT_THREADS) {
                 const int h = t / half, i = t % half;
@@ -122,54 +122,38 @@ ES_DEV void attn_item(const AttnArgs& a, int m, int jy, int sp) {
                 qs[h * ld + i + half] = (x1 * c + x0 * sn) * scale;
             }
         }
-        if (cached) {
 #pragma unroll
-            for (int u = 0; u < VPT; ++u) {
-                const int t = base + u * ATT_THREADS + tid;
-                if (t < nv) {
-                    float kf[EPV], vf[EPV];
-                    unpack16(kv4[u], kf, T());
-                    unpack16(vv4[u], vf, T());
-                    const int i = t * EPV / hd, e = t * EPV % hd;
+        for (int u = 0; u < VPT; ++u) {
+            const int t = base + u * ATT_THREADS + tid;
+            if (t < nv) {
+                float kf[EPV], vf[EPV];
+                unpack16(kv4[u], kf, T());
+                unpack16(vv4[u], vf, T());
+                const int i = t * EPV / hd, e = t * EPV % hd;
 #pragma unroll
-                    for (int x = 0; x < EPV; ++x) { ks[i * ld + e + x] = kf[x]; vs[i * ld + e + x] = vf[x]; }
-                }
+                for (int x = 0; x < EPV; ++x) { ks[i * ld + e + x] = kf[x]; vs[i * ld + e + x] = vf[x]; }
             }
         }
-        if (!cached) break;
     }
-    if (!cached) {
-        // the split holding this launch's own rows: cached positions before
-        // bpos, the launch's raw k/v rows (rotated, rounded to the cache
-        // type as a cached entry would be) from bpos on
-        for (int t = tid; t < n * half; t += ATT_THREADS) {
-            const int i = t / half, e = t % half, p = p0 + i;
-            float k0, k1, v0, v1;
-            if (p < bpos) {
-                const T* kr = kv_ptr<T>(a.g, seq, p, layer, 0, hk);
-                const T* vr = kv_ptr<T>(a.g, seq, p, layer, 1, hk);
-                k0 = ldcg_f(kr + e); k1 = ldcg_f(kr + e + half);
-                v0 = ldcg_f(vr + e); v1 = ldcg_f(vr + e + half);
-            } else {
-                const size_t r = (size_t)(rb + (p - bpos)) * kvd + (size_t)hk * hd;
-                const float* cs = a.rope + (size_t)p * hd;
-                const float c = cs[2 * e], sn = cs[2 * e + 1];
-                const float x0 = __ldcg(a.k[j] + r + e), x1 = __ldcg(a.k[j] + r + e + half);
-                k0 = to_f32(from_f32<T>(x0 * c - x1 * sn));
-                k1 = to_f32(from_f32<T>(x1 * c + x0 * sn));
-                v0 = to_f32(from_f32<T>(__ldcg(a.v[j] + r + e)));
-                v1 = to_f32(from_f32<T>(__ldcg(a.v[j] + r + e + half)));
-            }
-            ks[i * ld + e] = k0; ks[i * ld + e + half] = k1;
-            vs[i * ld + e] = v0; vs[i * ld + e + half] = v1;
-        }
+    // the launch's own positions (from bpos on): its raw k/v rows, rotated
+    // and rounded to the cache type as a cached entry would be
+    for (int t = tid; t < (n - ncached) * half; t += ATT_THREADS) {
+        const int i = ncached + t / half, e = t % half, p = p0 + i;
+        const size_t r = (size_t)(rb + (p - bpos)) * kvd + (size_t)hk * hd;
+        const float* cs = a.rope + (size_t)p * hd;
+        const float c = cs[2 * e], sn = cs[2 * e + 1];
+        const float x0 = __ldcg(a.k[j] + r + e), x1 = __ldcg(a.k[j] + r + e + half);
+        ks[i * ld + e] = to_f32(from_f32<T>(x0 * c - x1 * sn));
+        ks[i * ld + e + half] = to_f32(from_f32<T>(x1 * c + x0 * sn));
+        vs[i * ld + e] = to_f32(from_f32<T>(__ldcg(a.v[j] + r + e)));
+        vs[i * ld + e + half] = to_f32(from_f32<T>(__ldcg(a.v[j] + r + e + half)));
     }
     __syncthreads();
     // append this row's own entry (it lies in this split when p0 <= pos)
     if (pos < p0 + n && pos >= bpos) {
         const int i = pos - p0;
-        T* kd = kv_ptr<T>(a.g, seq, pos, layer, 0, hk);
-        T* vd = kv_ptr<T>(a.g, seq, pos, layer, 1, hk);
+        T* kd = (T*)a.g.kv + kvoff + (size_t)i * hd;
+        T* vd = kd + (size_t)Hkv * PAGE * hd;
         for (int e = tid; e < hd; e += ATT_THREADS) {
             kd[e] = from_f32<T>(ks[i * ld + e]);
             vd[e] = from_f32<T>(vs[i * ld + e]);

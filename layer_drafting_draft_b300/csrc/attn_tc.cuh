@@ -52,14 +52,20 @@ ES_DEV void mma16816(float (&d)[4], const uint32_t* a, uint32_t b0, uint32_t b1)
 template <int HD>
 __global__ void __launch_bounds__(ATC_THREADS) attn_tc_kernel(AttnArgs a) {
     extern __shared__ __align__(16) unsigned char atc_smem[];
-    __shared__ int s_pos[ATC_QV];
+    __shared__ int s_pos[ATC_QV];   // position of each query vector's row (-1: none)
+    __shared__ int s_rp[ATC_QV];    // positions of the group's rows
+    __shared__ int s_meta[3];       // the block's first row, the sequence, the chunk's first page
     constexpr int LD = HD + 8, LDV = PAGE + 8, HALF = HD / 2;
+    constexpr int VPR = HD / 8;                    // 16-byte vectors of a K or V row
+    constexpr int NV = PAGE * VPR / ATC_THREADS;   // of a page, per thread
+    constexpr int QV4 = HALF / 4;                  // items (4 dimensions and their partners) per vector
+    constexpr int QB = 4;                          // items per thread whose loads are in flight together
     bf16* qhi = reinterpret_cast<bf16*>(atc_smem);
     bf16* qlo = qhi + ATC_QV * LD;
     bf16* ks = qlo + ATC_QV * LD;
     bf16* vt = ks + PAGE * LD;
 
-    const int Hkv = a.g.Hkv, G = a.H / Hkv;
+    const int Hkv = a.g.Hkv, G = a.H / Hkv, pps = a.g.pages_per_seq;
     const int gps = (a.rps + a.rg - 1) / a.rg;
     const int sq = blockIdx.x / gps, gi = blockIdx.x % gps;
     const int m0 = sq * a.rps + gi * a.rg, nr = min(a.rg, a.rps - gi * a.rg);
@@ -68,58 +74,114 @@ __global__ void __launch_bounds__(ATC_THREADS) attn_tc_kernel(AttnArgs a) {
     const int layer = a.layer[j];
     const int kvd = Hkv * HD, qd = a.H * HD;
     const int nq = nr * G;                       // query vectors (row-major: r * G + h)
-    // rows of the group: positions (-1: inactive row) and the sequence block
-    int maxpos = -1;
-    for (int r = 0; r < nr; ++r) maxpos = max(maxpos, __ldcg(a.row_pos + m0 + r));
+    // The descriptors in one round of independent loads: the rows' positions
+    // (-1: inactive row), the block's first row and the sequence.  Rows are
+    // laid out sequence by sequence, so the group's sequence is the launch's
+    // sq-th and the chunk's first page can be looked up at the same time
+    // (again below if row_seq says otherwise).
+    if (tid < nr) s_rp[tid] = __ldcg(a.row_pos + m0 + tid);
+    if (tid == ATC_THREADS - 1) s_meta[0] = __ldcg(a.row_base + m0);
+    if (tid == ATC_THREADS - 2) s_meta[1] = __ldcg(a.row_seq + m0);
+    if (tid == ATC_THREADS - 3)
+        s_meta[2] = ch * a.ppc < pps ? __ldcg(a.g.page_table + (size_t)sq * pps + ch * a.ppc) : -1;
+    __syncthreads();
+    int maxpos = -1, ra = -1;
+    for (int r = 0; r < nr; ++r) {
+        const int p = s_rp[r];
+        maxpos = max(maxpos, p);
+        if (ra < 0 && p >= 0) ra = r;
+    }
     const int npg = maxpos / PAGE + 1;           // pages of the group
     const int pg0 = ch * a.ppc, pg1 = min(npg, pg0 + a.ppc);
     if (maxpos < 0 || pg0 >= npg) return;
     const int nch = (npg + a.ppc - 1) / a.ppc;   // chunks of the group
-    const int rb = __ldcg(a.row_base + m0), bpos = __ldcg(a.row_pos + rb), seq = __ldcg(a.row_seq + m0);
-    if (tid < ATC_QV) s_pos[tid] = tid < nq ? __ldcg(a.row_pos + m0 + tid / G) : -1;
-    __syncthreads();
+    const int rb = s_meta[0], seq = s_meta[1];
+    // the rows of a block hold consecutive positions from its first row on
+    const int bpos = s_rp[ra] - (m0 + ra - rb);
+    int page = seq == sq ? s_meta[2] : a.g.page_table[(size_t)seq * pps + pg0];
+    if (tid < ATC_QV) s_pos[tid] = tid < nq ? s_rp[tid / G] : -1;
 
-    // cached part of a page (written by earlier launches)
-    auto load_cached = [&](int p0, int ncached) {
-        const bf16* Kp = kv_ptr<bf16>(a.g, seq, p0, layer, 0, hk);
-        const bf16* Vp = kv_ptr<bf16>(a.g, seq, p0, layer, 1, hk);
-        for (int t = tid; t < ncached * (HD / 8); t += ATC_THREADS) {
-            const int i = t / (HD / 8), e = (t % (HD / 8)) * 8;
-            const uint4 kk = __ldcg(reinterpret_cast<const uint4*>(Kp + (size_t)i * HD + e));
-            const uint4 vv = __ldcg(reinterpret_cast<const uint4*>(Vp + (size_t)i * HD + e));
-            *reinterpret_cast<uint4*>(ks + i * LD + e) = kk;
-            const bf16* vb = reinterpret_cast<const bf16*>(&vv);
+    // K and V of (page, this layer, this kv head)
+    auto page_kv = [&](int pid, int kv) {
+        return reinterpret_cast<bf16*>(a.g.kv) + ((((size_t)pid * a.g.L + layer) * 2 + kv) * Hkv + hk) * PAGE * HD;
+    };
+    // cached part of a page (written by earlier launches): 16-byte loads
+    // into registers, then K row-major and V transposed into shared memory
+    uint4 kk[NV], vv[NV];
+    auto issue_cached = [&](int pid, int ncached) {
+        const uint4* Kp = reinterpret_cast<const uint4*>(page_kv(pid, 0));
+        const uint4* Vp = reinterpret_cast<const uint4*>(page_kv(pid, 1));
 #pragma unroll
-            for (int x = 0; x < 8; ++x) vt[(e + x) * LDV + i] = vb[x];
+        for (int u = 0; u < NV; ++u) {
+            const int t = u * ATC_THREADS + tid;
+            if (t < ncached * VPR) {
+                kk[u] = __ldcg(Kp + t);
+                vv[u] = __ldcg(Vp + t);
+            }
+        }
+    };
+    auto store_cached = [&](int ncached) {
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+            const int t = u * ATC_THREADS + tid;
+            if (t < ncached * VPR) {
+                const int i = t / VPR, e = (t % VPR) * 8;
+                *reinterpret_cast<uint4*>(ks + i * LD + e) = kk[u];
+                const bf16* vb = reinterpret_cast<const bf16*>(&vv[u]);
+#pragma unroll
+                for (int x = 0; x < 8; ++x) vt[(e + x) * LDV + i] = vb[x];
+            }
         }
     };
     // the first page's cached part is requested before waiting for the
     // preceding kernel
     {
         const int p0 = pg0 * PAGE, n = min(PAGE, maxpos + 1 - p0);
-        load_cached(p0, max(0, min(n, bpos - p0)));
+        issue_cached(page, max(0, min(n, bpos - p0)));
     }
     grid_dep_wait();
     grid_dep_launch();
     // queries: rotated to their row's position, scaled, split hi/lo
     const float scale = 1.0f / sqrtf((float)HD);
-    for (int t = tid; t < ATC_QV * HALF; t += ATC_THREADS) {
-        const int v = t / HALF, e = t % HALF;
-        float y0 = 0.f, y1 = 0.f;
-        if (v < nq && s_pos[v] >= 0) {
-            const int r = v / G, h = v % G, pos = s_pos[v];
-            const float* q = a.q[j] + (size_t)(m0 + r) * qd + (size_t)(hk * G + h) * HD;
-            const float* cs = a.rope + (size_t)pos * HD;
-            const float c = cs[2 * e], sn = cs[2 * e + 1];
-            const float x0 = __ldcg(q + e), x1 = __ldcg(q + e + HALF);
-            y0 = (x0 * c - x1 * sn) * scale;
-            y1 = (x1 * c + x0 * sn) * scale;
+#pragma unroll 1
+    for (int t0 = 0; t0 < ATC_QV * QV4; t0 += QB * ATC_THREADS) {
+        float4 x0[QB], x1[QB], cA[QB], cB[QB];
+#pragma unroll
+        for (int u = 0; u < QB; ++u) {
+            const int t = t0 + u * ATC_THREADS + tid, v = t / QV4, e = (t % QV4) * 4;
+            const int pos = v < nq ? s_rp[v / G] : -1;
+            x0[u] = x1[u] = cA[u] = cB[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (pos >= 0) {
+                const float* q = a.q[j] + (size_t)(m0 + v / G) * qd + (size_t)(hk * G + v % G) * HD;
+                const float* cs = a.rope + (size_t)pos * HD;
+                x0[u] = __ldcg(reinterpret_cast<const float4*>(q + e));
+                x1[u] = __ldcg(reinterpret_cast<const float4*>(q + e + HALF));
+                cA[u] = __ldg(reinterpret_cast<const float4*>(cs + 2 * e));
+                cB[u] = __ldg(reinterpret_cast<const float4*>(cs + 2 * e + 4));
+            }
         }
-        const bf16 h0 = __float2bfloat16_rn(y0), h1 = __float2bfloat16_rn(y1);
-        qhi[v * LD + e] = h0;
-        qhi[v * LD + e + HALF] = h1;
-        qlo[v * LD + e] = __float2bfloat16_rn(y0 - __bfloat162float(h0));
-        qlo[v * LD + e + HALF] = __float2bfloat16_rn(y1 - __bfloat162float(h1));
+        if (t0 == 0) {   // the cached page has arrived meanwhile
+            const int p0 = pg0 * PAGE, n = min(PAGE, maxpos + 1 - p0);
+            store_cached(max(0, min(n, bpos - p0)));
+        }
+#pragma unroll
+        for (int u = 0; u < QB; ++u) {
+            const int t = t0 + u * ATC_THREADS + tid, v = t / QV4, e = (t % QV4) * 4;
+            const float xa[4] = {x0[u].x, x0[u].y, x0[u].z, x0[u].w};
+            const float xb[4] = {x1[u].x, x1[u].y, x1[u].z, x1[u].w};
+            const float c[4] = {cA[u].x, cA[u].z, cB[u].x, cB[u].z};
+            const float sn[4] = {cA[u].y, cA[u].w, cB[u].y, cB[u].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float y0 = (xa[k] * c[k] - xb[k] * sn[k]) * scale;
+                const float y1 = (xb[k] * c[k] + xa[k] * sn[k]) * scale;
+                const bf16 h0 = __float2bfloat16_rn(y0), h1 = __float2bfloat16_rn(y1);
+                qhi[v * LD + e + k] = h0;
+                qhi[v * LD + e + k + HALF] = h1;
+                qlo[v * LD + e + k] = __float2bfloat16_rn(y0 - __bfloat162float(h0));
+                qlo[v * LD + e + k + HALF] = __float2bfloat16_rn(y1 - __bfloat162float(h1));
+            }
+        }
     }
 
     const int g = lane >> 2, cq = lane & 3;
@@ -134,19 +196,56 @@ __global__ void __launch_bounds__(ATC_THREADS) attn_tc_kernel(AttnArgs a) {
         const int ncached = max(0, min(n, bpos - p0));
         if (pg > pg0) {
             __syncthreads();   // every warp is done with the previous page
-            load_cached(p0, ncached);
+            page = a.g.page_table[(size_t)seq * pps + pg];
+            // later pages of a multi-page chunk: copied without the register
+            // staging, which would compete with the running output here
+            const uint4* Kp = reinterpret_cast<const uint4*>(page_kv(page, 0));
+            const uint4* Vp = reinterpret_cast<const uint4*>(page_kv(page, 1));
+            for (int t = tid; t < ncached * VPR; t += ATC_THREADS) {
+                const int i = t / VPR, e = (t % VPR) * 8;
+                const uint4 kv = __ldcg(Kp + t), vv1 = __ldcg(Vp + t);
+                *reinterpret_cast<uint4*>(ks + i * LD + e) = kv;
+                const bf16* vb = reinterpret_cast<const bf16*>(&vv1);
+#pragma unroll
+                for (int x = 0; x < 8; ++x) vt[(e + x) * LDV + i] = vb[x];
+            }
         }
         // the launch's own positions (>= bpos): rotate and round the raw rows
-        for (int t = tid; t < (n - ncached) * HALF; t += ATC_THREADS) {
-            const int i = ncached + t / HALF, e = t % HALF, p = p0 + i;
-            const size_t r = (size_t)(rb + (p - bpos)) * kvd + (size_t)hk * HD;
-            const float* cs = a.rope + (size_t)p * HD;
-            const float c = cs[2 * e], sn = cs[2 * e + 1];
-            const float x0 = __ldcg(a.k[j] + r + e), x1 = __ldcg(a.k[j] + r + e + HALF);
-            ks[i * LD + e] = __float2bfloat16_rn(x0 * c - x1 * sn);
-            ks[i * LD + e + HALF] = __float2bfloat16_rn(x1 * c + x0 * sn);
-            vt[e * LDV + i] = __float2bfloat16_rn(__ldcg(a.v[j] + r + e));
-            vt[(e + HALF) * LDV + i] = __float2bfloat16_rn(__ldcg(a.v[j] + r + e + HALF));
+#pragma unroll 1
+        for (int t0 = 0; t0 < (n - ncached) * QV4; t0 += 2 * ATC_THREADS) {
+            float4 k0[2], k1[2], w0[2], w1[2], cA[2], cB[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int t = t0 + u * ATC_THREADS + tid, i = ncached + t / QV4, e = (t % QV4) * 4, p = p0 + i;
+                if (t < (n - ncached) * QV4) {
+                    const size_t r = (size_t)(rb + (p - bpos)) * kvd + (size_t)hk * HD + e;
+                    const float* cs = a.rope + (size_t)p * HD + 2 * e;
+                    k0[u] = __ldcg(reinterpret_cast<const float4*>(a.k[j] + r));
+                    k1[u] = __ldcg(reinterpret_cast<const float4*>(a.k[j] + r + HALF));
+                    w0[u] = __ldcg(reinterpret_cast<const float4*>(a.v[j] + r));
+                    w1[u] = __ldcg(reinterpret_cast<const float4*>(a.v[j] + r + HALF));
+                    cA[u] = __ldg(reinterpret_cast<const float4*>(cs));
+                    cB[u] = __ldg(reinterpret_cast<const float4*>(cs + 4));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int t = t0 + u * ATC_THREADS + tid, i = ncached + t / QV4, e = (t % QV4) * 4;
+                if (t >= (n - ncached) * QV4) continue;
+                const float xa[4] = {k0[u].x, k0[u].y, k0[u].z, k0[u].w};
+                const float xb[4] = {k1[u].x, k1[u].y, k1[u].z, k1[u].w};
+                const float va[4] = {w0[u].x, w0[u].y, w0[u].z, w0[u].w};
+                const float vb[4] = {w1[u].x, w1[u].y, w1[u].z, w1[u].w};
+                const float c[4] = {cA[u].x, cA[u].z, cB[u].x, cB[u].z};
+                const float sn[4] = {cA[u].y, cA[u].w, cB[u].y, cB[u].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    ks[i * LD + e + k] = __float2bfloat16_rn(xa[k] * c[k] - xb[k] * sn[k]);
+                    ks[i * LD + e + k + HALF] = __float2bfloat16_rn(xb[k] * c[k] + xa[k] * sn[k]);
+                    vt[(e + k) * LDV + i] = __float2bfloat16_rn(va[k]);
+                    vt[(e + k + HALF) * LDV + i] = __float2bfloat16_rn(vb[k]);
+                }
+            }
         }
         // zero the tail of the page so the k16 steps read finite values
         for (int t = tid; t < (PAGE - n) * HD; t += ATC_THREADS) {
@@ -155,13 +254,20 @@ __global__ void __launch_bounds__(ATC_THREADS) attn_tc_kernel(AttnArgs a) {
             vt[e * LDV + i] = __float2bfloat16_rn(0.f);
         }
         __syncthreads();
-        // each row's own entry, when this page holds its position
-        for (int t = tid; t < nr * HD; t += ATC_THREADS) {
-            const int r = t / HD, e = t % HD, pos = __ldcg(a.row_pos + m0 + r);
+        // each row's own entry, when this page holds its position (16 bytes
+        // of K and of V per item)
+        for (int t = tid; t < nr * VPR; t += ATC_THREADS) {
+            const int r = t / VPR, e = (t % VPR) * 8, pos = s_rp[r];
             if (pos < bpos || pos < p0 || pos >= p0 + n) continue;
             const int i = pos - p0;
-            kv_ptr<bf16>(a.g, seq, pos, layer, 0, hk)[e] = ks[i * LD + e];
-            kv_ptr<bf16>(a.g, seq, pos, layer, 1, hk)[e] = vt[e * LDV + i];
+            *reinterpret_cast<uint4*>(page_kv(page, 0) + (size_t)i * HD + e) =
+                *reinterpret_cast<const uint4*>(ks + i * LD + e);
+            uint32_t w[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+                w[x] = (uint32_t)__bfloat16_as_ushort(vt[(e + 2 * x) * LDV + i]) |
+                       ((uint32_t)__bfloat16_as_ushort(vt[(e + 2 * x + 1) * LDV + i]) << 16);
+            *reinterpret_cast<uint4*>(page_kv(page, 1) + (size_t)i * HD + e) = make_uint4(w[0], w[1], w[2], w[3]);
         }
         if (!active) continue;
         // S = Q K^T for this page (one 16-vector tile per warp)
@@ -297,10 +403,14 @@ __global__ void __launch_bounds__(HD) attn_merge_kernel(AttnArgs a) {
     grid_dep_wait();
     grid_dep_launch();
     if (v >= nr * G) return;
+    // the group's row positions, loaded together (nr <= 64 <= HD)
+    __shared__ int s_rp[ATC_QV];
+    if (threadIdx.x < nr) s_rp[threadIdx.x] = __ldcg(a.row_pos + m0 + threadIdx.x);
+    __syncthreads();
     int maxpos = -1;
-    for (int r = 0; r < nr; ++r) maxpos = max(maxpos, __ldcg(a.row_pos + m0 + r));
+    for (int r = 0; r < nr; ++r) maxpos = max(maxpos, s_rp[r]);
     const int nch = maxpos < 0 ? 0 : (maxpos / PAGE + 1 + a.ppc - 1) / a.ppc;
-    const int r = v / G, h = v % G, pos = __ldcg(a.row_pos + m0 + r);
+    const int r = v / G, h = v % G, pos = s_rp[r];
     if (nch <= 1 || pos < 0) return;
     const int na = (pos / PAGE + 1 + a.ppc - 1) / a.ppc;   // chunks this row sees
     const float* pp = a.part + (((size_t)(m0 + r) * a.nl + j) * a.H + (size_t)hk * G + h) * a.nsplit * (HD + 2);

@@ -756,11 +756,14 @@ Rec attn_rec(es_ctx* c, Model& m, int l0, int n, int M, int rps) {
     r.bf16 = m.dtype == ES_DTYPE_BF16;
     r.smem = (int)attn_smem_bytes(m.H / m.Hkv, m.hd, m.nsplit);
     r.M = M;
+    // rows laid out as M / rps sequences of rps rows: the kernels take row m's
+    // sequence to be m / rps when they look up its first page (an index into
+    // the max_batch sequences' page table)
+    a.rps = rps >= 1 && M % rps == 0 && M / rps <= c->cfg.max_batch ? rps : 0;
     const int G = m.H / m.Hkv;
     const int rg = std::max(1, ATC_QV / G);
-    const int groups = rps >= 1 && M % rps == 0 ? (M / rps) * ((rps + rg - 1) / rg) * n * m.Hkv : 0;
-    if (r.bf16 && rps >= 2 && M % rps == 0 && (m.hd == 64 || m.hd == 128) && groups * m.nsplit >= 64) {
-        a.rps = rps;
+    const int groups = a.rps ? (M / rps) * ((rps + rg - 1) / rg) * n * m.Hkv : 0;
+    if (r.bf16 && a.rps >= 2 && (m.hd == 64 || m.hd == 128) && groups * m.nsplit >= 64) {
         a.rg = rg;
         // pages per CTA: about four CTAs per SM over the cache's pages, and at
         // most 256 chunks (the merge kernel's weight buffer)
