@@ -669,45 +669,100 @@ __host__ __device__ inline int gvm_windows(const GvLaunch& L, int S0, int S1, Gv
     return n;
 }
 
-// Stage the windows with off >= 0 as hi/lo planes (whole CTA; synchronises).
-template <int SB, int NT>  // items per thread with their loads in flight together; threads
-ES_DEV void gvm_stage(const GvLaunch& L, const GvmWin* win, int nwin, int nitems, unsigned char* xsm,
-                      const float* srinv) {
+// Stage the windows with off >= 0 as hi/lo planes (whole CTA; synchronises):
+// float32 (normalised) activations split into hi/lo bf16.  A thread takes
+// float4 columns c, c + NT, ... numbered across the staged windows and loads
+// that column of every activation row at once; the window of a column is
+// found by a cursor that only moves forward, so a column costs its loads,
+// the splits and the stores.
+template <int NT>
+ES_DEV void gvm_stage(const GvLaunch& L, const GvmWin* win, int nwin, unsigned char* xsm, const float* srinv) {
+    constexpr int RB = GV_MAXM;
     const int M = L.M;
-    // item t -> (window, activation row m, column offset kr in the window)
-    auto locate = [&](int t, int& i, int& m, int& kr) {
-        i = 0;
-        while (win[i].off < 0 || t >= win[i].item0 + M * ((win[i].khi - win[i].klo) * (GVM_COLS / 4))) ++i;
-        const int C4 = (win[i].khi - win[i].klo) * (GVM_COLS / 4), r = t - win[i].item0;
-        m = r / C4;
-        kr = (r - m * C4) * 4;
-    };
-    for (int t0 = threadIdx.x; t0 < nitems; t0 += SB * NT) {
-        float4 v[SB];
+    int total = 0;
+    for (int w = 0; w < nwin; ++w)
+        if (win[w].off >= 0) total += (win[w].khi - win[w].klo) * (GVM_COLS / 4);
+    int w = 0, wbase = 0;  // window of the current column, flat index of its first column
+    for (int c = threadIdx.x; c < total; c += NT) {
+        while (win[w].off < 0 || c >= wbase + (win[w].khi - win[w].klo) * (GVM_COLS / 4)) {
+            if (win[w].off >= 0) wbase += (win[w].khi - win[w].klo) * (GVM_COLS / 4);
+            ++w;
+        }
+        const GvmWin& wn = win[w];
+        const GvXSrc& x = L.xs[wn.src];
+        const int kr = (c - wbase) * 4, k = wn.klo * GVM_COLS + kr;
+        bf16* hi = reinterpret_cast<bf16*>(xsm + (size_t)wn.off * 4) + kr;
+        for (int m0 = 0; m0 < M; m0 += RB) {
+            float4 v[RB];
 #pragma unroll
-        for (int u = 0; u < SB; ++u) {
+            for (int u = 0; u < RB; ++u) {
+                v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (m0 + u < M && k < x.K) v[u] = gvm_x4(x, m0 + u, k, srinv);
+            }
+#pragma unroll
+            for (int u = 0; u < RB; ++u) {
+                const int m = m0 + u;
+                if (m >= M) break;
+                uint2 h, l;
+                split2(v[u].x, v[u].y, h.x, l.x);
+                split2(v[u].z, v[u].w, h.y, l.y);
+                *reinterpret_cast<uint2*>(hi + (size_t)m * wn.pw) = h;
+                *reinterpret_cast<uint2*>(hi + (size_t)(M + m) * wn.pw) = l;
+            }
+        }
+    }
+    __syncthreads();
+}
+
+// The same for a CTA with few stages (small windows) that holds both ring
+// stages while staging: (row, column) items spread over all threads, two
+// per thread with their loads in flight together.
+template <int NT>
+ES_DEV void gvm_stage_small(const GvLaunch& L, const GvmWin* win, int nwin, unsigned char* xsm,
+                            const float* srinv) {
+    const int M = L.M;
+    int total = 0;
+    for (int w = 0; w < nwin; ++w)
+        if (win[w].off >= 0) total += (win[w].khi - win[w].klo) * (GVM_COLS / 4);
+    // item t -> row t / total, flat column t % total -> (window, column in it)
+    auto locate = [&](int t, int& w, int& m, int& kr) {
+        m = t / total;
+        int c = t - m * total;
+        w = 0;
+        for (;; ++w) {
+            if (win[w].off < 0) continue;
+            const int C4 = (win[w].khi - win[w].klo) * (GVM_COLS / 4);
+            if (c < C4) break;
+            c -= C4;
+        }
+        kr = 4 * c;
+    };
+    for (int t0 = threadIdx.x; t0 < M * total; t0 += 2 * NT) {
+        float4 v[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
             const int t = t0 + u * NT;
             v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (t < nitems) {
-                int i, m, kr;
-                locate(t, i, m, kr);
-                const GvXSrc& x = L.xs[win[i].src];
-                const int k = win[i].klo * GVM_COLS + kr;
+            if (t < M * total) {
+                int w, m, kr;
+                locate(t, w, m, kr);
+                const GvXSrc& x = L.xs[win[w].src];
+                const int k = win[w].klo * GVM_COLS + kr;
                 if (k < x.K) v[u] = gvm_x4(x, m, k, srinv);
             }
         }
 #pragma unroll
-        for (int u = 0; u < SB; ++u) {
+        for (int u = 0; u < 2; ++u) {
             const int t = t0 + u * NT;
-            if (t >= nitems) break;
-            int i, m, kr;
-            locate(t, i, m, kr);
-            bf16* hi = reinterpret_cast<bf16*>(xsm + (size_t)win[i].off * 4) + (size_t)m * win[i].pw + kr;
+            if (t >= M * total) break;
+            int w, m, kr;
+            locate(t, w, m, kr);
+            bf16* hi = reinterpret_cast<bf16*>(xsm + (size_t)win[w].off * 4) + (size_t)m * win[w].pw + kr;
             uint2 h, l;
             split2(v[u].x, v[u].y, h.x, l.x);
             split2(v[u].z, v[u].w, h.y, l.y);
             *reinterpret_cast<uint2*>(hi) = h;
-            *reinterpret_cast<uint2*>(hi + (size_t)M * win[i].pw) = l;
+            *reinterpret_cast<uint2*>(hi + (size_t)M * win[w].pw) = l;
         }
     }
     __syncthreads();
@@ -1029,15 +1084,21 @@ gvm_kernel(const GvLaunch* __restrict__ Lg, float* __restrict__ scratch, int* __
     __syncthreads();
     grid_dep_wait();
     grid_dep_launch();
-    // the ring's other stage goes out before the staging round trips
-#pragma unroll
-    for (int i = GVM_D - 1; i < GVM_D; ++i)
-        if (s_issue < S1) { gvm_issue_step<NW>(L, ws, I, ring[i], S1); ++s_issue; }
     const int nwin = s_nwin;
     {
         GvmRinv R;
         gvm_rinv_issue(L, R);
-        gvm_stage<8, NW * 32>(L, win, nwin, s_items, gvm_xsm, srinv);  // ends with a barrier
+        // The ring's other stage: with more stages to come it goes out once
+        // the staging loads are done (issued earlier, its loads queue ahead
+        // of them); a CTA whose stages all fit the ring issues it first, so
+        // that its latency hides behind the staging.
+        if (S1 - S0 <= GVM_D) {
+            if (s_issue < S1) { gvm_issue_step<NW>(L, ws, I, ring[GVM_D - 1], S1); ++s_issue; }
+            gvm_stage_small<NW * 32>(L, win, nwin, gvm_xsm, srinv);  // ends with a barrier
+        } else {
+            gvm_stage<NW * 32>(L, win, nwin, gvm_xsm, srinv);  // ends with a barrier
+            if (s_issue < S1) { gvm_issue_step<NW>(L, ws, I, ring[GVM_D - 1], S1); ++s_issue; }
+        }
         gvm_rinv_finish(L, R, srinv);
         __syncthreads();
     }
