@@ -393,8 +393,7 @@ __global__ void __launch_bounds__(ATC_THREADS) attn_tc_kernel(AttnArgs a) {
 // chunk order.  Groups that fit one chunk were finished by attn_tc_kernel.
 template <int HD>
 __global__ void __launch_bounds__(HD) attn_merge_kernel(AttnArgs a) {
-    __shared__ float wsh[256];
-    __shared__ float red[32];
+    __shared__ float s_m[256], s_l[256];   // the chunks' max and sum (at most 256 chunks)
     const int Hkv = a.g.Hkv, G = a.H / Hkv;
     const int gps = (a.rps + a.rg - 1) / a.rg;
     const int sq = blockIdx.x / gps, gi = blockIdx.x % gps;
@@ -415,21 +414,33 @@ __global__ void __launch_bounds__(HD) attn_merge_kernel(AttnArgs a) {
     const int na = (pos / PAGE + 1 + a.ppc - 1) / a.ppc;   // chunks this row sees
     const float* pp = a.part + (((size_t)(m0 + r) * a.nl + j) * a.H + (size_t)hk * G + h) * a.nsplit * (HD + 2);
     const int tid = threadIdx.x;
-    float mx = -INFINITY;
-    for (int c = tid; c < na; c += HD) mx = fmaxf(mx, __ldcg(pp + (size_t)c * (HD + 2) + HD));
-    mx = block_max(mx, red);
-    float den = 0.f;
+    // every chunk's max and sum, and this thread's output element of the
+    // first NB chunks, in one round of loads
+    constexpr int NB = 16;
     for (int c = tid; c < na; c += HD) {
-        const float mc = __ldcg(pp + (size_t)c * (HD + 2) + HD);
-        const float wc = mc == -INFINITY ? 0.f : expf(mc - mx);
-        if (c < 256) wsh[c] = wc;
-        den = fmaf(wc, __ldcg(pp + (size_t)c * (HD + 2) + HD + 1), den);
+        s_m[c] = __ldcg(pp + (size_t)c * (HD + 2) + HD);
+        s_l[c] = __ldcg(pp + (size_t)c * (HD + 2) + HD + 1);
     }
-    den = block_sum(den, red);
+    float oc[NB];
+#pragma unroll
+    for (int c = 0; c < NB; ++c) oc[c] = c < na ? __ldcg(pp + (size_t)c * (HD + 2) + tid) : 0.f;
     __syncthreads();
-    float num = 0.f;
-#pragma unroll 8
-    for (int c = 0; c < na; ++c) num = fmaf(wsh[c], __ldcg(pp + (size_t)c * (HD + 2) + tid), num);
+    float mx = -INFINITY;
+    for (int c = 0; c < na; ++c) mx = fmaxf(mx, s_m[c]);
+    // weights w_c = exp(m_c - max), summed with the outputs in chunk order
+    float den = 0.f, num = 0.f;
+#pragma unroll
+    for (int c = 0; c < NB; ++c) {
+        if (c >= na) break;
+        const float wc = s_m[c] == -INFINITY ? 0.f : expf(s_m[c] - mx);
+        den = fmaf(wc, s_l[c], den);
+        num = fmaf(wc, oc[c], num);
+    }
+    for (int c = NB; c < na; ++c) {
+        const float wc = s_m[c] == -INFINITY ? 0.f : expf(s_m[c] - mx);
+        den = fmaf(wc, s_l[c], den);
+        num = fmaf(wc, __ldcg(pp + (size_t)c * (HD + 2) + tid), num);
+    }
     a.out[j][(size_t)(m0 + r) * (a.H * HD) + (size_t)(hk * G + h) * HD + tid] = num / den;
 }
 

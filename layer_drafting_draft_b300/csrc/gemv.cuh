@@ -1045,7 +1045,19 @@ ES_DEV void gvm_rinv_finish(const GvLaunch& L, const GvmRinv& R, float* srinv) {
     float t = 0.f;
 #pragma unroll
     for (int u = 0; u < 8; ++u) t += R.r[u];
-    for (int i = lane + 256; i < x.ss_tiles; i += 32) t += __ldcg(x.rinv + (size_t)i * x.ss_ld + pr);
+    // further partials (more than 256 tiles) in batches of 8 loads in flight,
+    // added in the same lane-strided order
+    for (int i0 = lane + 256; i0 < x.ss_tiles; i0 += 256) {
+        float r[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + 32 * u;
+            r[u] = i < x.ss_tiles ? __ldcg(x.rinv + (size_t)i * x.ss_ld + pr) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (i0 + 32 * u < x.ss_tiles) t += r[u];
+    }
     t = warp_sum(t);
     if (lane == 0) srinv[warp] = 1.0f / sqrtf(t / (float)x.K + x.eps);
 }
