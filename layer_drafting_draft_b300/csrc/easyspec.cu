@@ -23,6 +23,7 @@
 #include "../../include/easyspec.h"
 #include "kernels.cuh"
 #include "tcgemm.cuh"
+#include "planes.cuh"
 #include "attn_tc.cuh"
 
 using namespace es;
@@ -723,6 +724,12 @@ Rec norm_planes_rec(Model& m, const float* add, const void* gain, bf16* dst, int
     a.h = m.h; a.add = add; a.g = (const bf16*)gain; a.dst = dst; a.d = m.d; a.M = rows;
     a.src_stride = stride; a.src_off = off; a.eps = m.eps;
     a.ssp = ssp; a.ss_tiles = ss_tiles; a.ss_ld = ss_ld;
+    // the kernel moves 4 columns per thread (16-byte rows, 8-byte planes)
+    if (m.d % 4 || (uintptr_t)dst % 16 || (uintptr_t)m.h % 16 || (add && (uintptr_t)add % 16))
+        arg_fail(ES_ERR_ARG, "internal: normalised planes need 4-column aligned rows");
+    // without partial sums every CTA sums the whole row of h + add, which
+    // the CTAs also write back: only a row without `add` may take that path
+    if (add && !ssp) arg_fail(ES_ERR_ARG, "internal: normalised planes with an addend need partial sums");
     r.g3 = dim3(rows, (m.d + NPL_COLS - 1) / NPL_COLS);
     return r;
 }

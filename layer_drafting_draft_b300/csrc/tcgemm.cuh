@@ -171,101 +171,6 @@ __host__ __device__ inline TcUnit tc_unit(const TcLaunch& L, int block) {
     return u;
 }
 
-// Activation planes: for source i, rows r*row_stride + row_off of src
-// (leading dimension ld, K columns) become hi/lo bf16 planes
-// dst[0][r][k], dst[1][r][k] ([2][M][K]).
-struct SplitArgs {
-    const float* src[TC_MAX_SRCS];
-    bf16* dst[TC_MAX_SRCS];
-    int ld[TC_MAX_SRCS], rs[TC_MAX_SRCS], ro[TC_MAX_SRCS], K[TC_MAX_SRCS];
-    int item0[TC_MAX_SRCS + 1];  // prefix of M*K/4 items per source
-    int nsrc, M;
-};
-
-__global__ void split_planes_kernel(SplitArgs a) {
-    grid_dep_wait();
-    grid_dep_launch();
-    const int total = a.item0[a.nsrc];
-    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < total; t += gridDim.x * blockDim.x) {
-        int i = 0;
-        while (t >= a.item0[i + 1]) ++i;
-        const int K4 = a.K[i] >> 2, u = t - a.item0[i];
-        const int m = u / K4, k = (u - m * K4) * 4;
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(
-            a.src[i] + (size_t)(m * a.rs[i] + a.ro[i]) * a.ld[i] + k));
-        const __nv_bfloat162 h0 = __floats2bfloat162_rn(v.x, v.y), h1 = __floats2bfloat162_rn(v.z, v.w);
-        const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
-        const __nv_bfloat162 l0 = __floats2bfloat162_rn(v.x - f0.x, v.y - f0.y);
-        const __nv_bfloat162 l1 = __floats2bfloat162_rn(v.z - f1.x, v.w - f1.y);
-        const size_t plane = (size_t)a.M * a.K[i];
-        __nv_bfloat162* ph = reinterpret_cast<__nv_bfloat162*>(a.dst[i] + (size_t)m * a.K[i] + k);
-        __nv_bfloat162* pl = reinterpret_cast<__nv_bfloat162*>(a.dst[i] + plane + (size_t)m * a.K[i] + k);
-        ph[0] = h0; ph[1] = h1; pl[0] = l0; pl[1] = l1;
-    }
-}
-
-// Normalised activation planes for a tensor-core pass that follows a
-// decode-size weight pass: row r reads h[src] (src = r*stride + off; if `add`
-// is set, h[src] += add[src] first, written back), takes
-// rinv = 1 / sqrt(mean(h^2) + eps) and writes the hi/lo planes of
-// h * rinv * gain to dst[0][r][.], dst[1][r][.] ([2][M][d]), the values the
-// RMSNorm kernel would store in float32.  Grid (rows, column chunks of
-// NPL_COLS): the mean comes from the producing pass's per-tile sums of
-// squares (ss_tiles partials of the source row at ssp[t * ss_ld + src],
-// added by one warp lane-strided and then in a fixed shuffle order, so every
-// chunk of a row gets the same value), or, without them, from the row
-// itself.
-constexpr int NPL_COLS = 1024;
-struct NormPlanesArgs {
-    float* h; const float* add; const bf16* g; bf16* dst;
-    const float* ssp; int ss_tiles, ss_ld;
-    int d, M, src_stride, src_off;
-    float eps;
-};
-__global__ void norm_planes_kernel(NormPlanesArgs a) {
-    __shared__ float red[32];
-    __shared__ float s_rinv;
-    grid_dep_wait();
-    const int r = blockIdx.x, tid = threadIdx.x;
-    const size_t src = (size_t)r * a.src_stride + a.src_off;
-    float* hr = a.h + src * a.d;
-    const int c0 = blockIdx.y * NPL_COLS, c1 = min(a.d, c0 + NPL_COLS);
-    if (a.ssp) {
-        if (tid < 32) {
-            float t = 0.f;
-            for (int i = tid; i < a.ss_tiles; i += 32) t += __ldcg(a.ssp + (size_t)i * a.ss_ld + src);
-            t = warp_sum(t);
-            if (tid == 0) s_rinv = 1.0f / sqrtf(t / (float)a.d + a.eps);
-        }
-        __syncthreads();
-    } else {
-        float ss = 0.f;
-        for (int i = tid; i < a.d; i += blockDim.x) {
-            float v = hr[i];
-            if (a.add) v += a.add[src * a.d + i];
-            ss += v * v;
-        }
-        ss = block_sum(ss, red);
-        if (tid == 0) s_rinv = 1.0f / sqrtf(ss / (float)a.d + a.eps);
-        __syncthreads();
-    }
-    grid_dep_launch();
-    const float rinv = s_rinv;
-    bf16* hi = a.dst + (size_t)r * a.d;
-    bf16* lo = hi + (size_t)a.M * a.d;
-    for (int i = c0 + tid; i < c1; i += blockDim.x) {
-        float v = hr[i];
-        if (a.add) {
-            v += a.add[src * a.d + i];
-            hr[i] = v;
-        }
-        const float x = v * rinv * __bfloat162float(a.g[i]);
-        const bf16 hb = __float2bfloat16_rn(x);
-        hi[i] = hb;
-        lo[i] = __float2bfloat16_rn(x - __bfloat162float(hb));
-    }
-}
-
 // ------------------------------------------------------------ PTX wrappers
 ES_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
