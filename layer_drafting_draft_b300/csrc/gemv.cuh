@@ -669,6 +669,36 @@ __host__ __device__ inline int gvm_windows(const GvLaunch& L, int S0, int S1, Gv
     return n;
 }
 
+// Float4 columns of the staged windows (off >= 0), numbered window by window.
+__host__ __device__ inline int gvm_stage_columns(const GvmWin* win, int nwin) {
+    int total = 0;
+    for (int w = 0; w < nwin; ++w)
+        if (win[w].off >= 0) total += (win[w].khi - win[w].klo) * (GVM_COLS / 4);
+    return total;
+}
+// Moves the cursor (window w, whose first column is wbase) to the staged
+// window holding column c < the total; c must not decrease between calls.
+__host__ __device__ inline void gvm_stage_cursor(const GvmWin* win, int c, int& w, int& wbase) {
+    while (win[w].off < 0 || c >= wbase + (win[w].khi - win[w].klo) * (GVM_COLS / 4)) {
+        if (win[w].off >= 0) wbase += (win[w].khi - win[w].klo) * (GVM_COLS / 4);
+        ++w;
+    }
+}
+// Item t < M * total of the small-window staging: activation row m =
+// t / total, and the window w and first element kr of flat column t % total.
+__host__ __device__ inline void gvm_stage_item(const GvmWin* win, int total, int t, int& w, int& m, int& kr) {
+    m = t / total;
+    int c = t - m * total;
+    w = 0;
+    for (;; ++w) {
+        if (win[w].off < 0) continue;
+        const int C4 = (win[w].khi - win[w].klo) * (GVM_COLS / 4);
+        if (c < C4) break;
+        c -= C4;
+    }
+    kr = 4 * c;
+}
+
 // Stage the windows with off >= 0 as hi/lo planes (whole CTA; synchronises):
 // float32 (normalised) activations split into hi/lo bf16.  A thread takes
 // float4 columns c, c + NT, ... numbered across the staged windows and loads
@@ -679,15 +709,10 @@ template <int NT>
 ES_DEV void gvm_stage(const GvLaunch& L, const GvmWin* win, int nwin, unsigned char* xsm, const float* srinv) {
     constexpr int RB = GV_MAXM;
     const int M = L.M;
-    int total = 0;
-    for (int w = 0; w < nwin; ++w)
-        if (win[w].off >= 0) total += (win[w].khi - win[w].klo) * (GVM_COLS / 4);
+    const int total = gvm_stage_columns(win, nwin);
     int w = 0, wbase = 0;  // window of the current column, flat index of its first column
     for (int c = threadIdx.x; c < total; c += NT) {
-        while (win[w].off < 0 || c >= wbase + (win[w].khi - win[w].klo) * (GVM_COLS / 4)) {
-            if (win[w].off >= 0) wbase += (win[w].khi - win[w].klo) * (GVM_COLS / 4);
-            ++w;
-        }
+        gvm_stage_cursor(win, c, w, wbase);
         const GvmWin& wn = win[w];
         const GvXSrc& x = L.xs[wn.src];
         const int kr = (c - wbase) * 4, k = wn.klo * GVM_COLS + kr;
@@ -721,22 +746,7 @@ template <int NT>
 ES_DEV void gvm_stage_small(const GvLaunch& L, const GvmWin* win, int nwin, unsigned char* xsm,
                             const float* srinv) {
     const int M = L.M;
-    int total = 0;
-    for (int w = 0; w < nwin; ++w)
-        if (win[w].off >= 0) total += (win[w].khi - win[w].klo) * (GVM_COLS / 4);
-    // item t -> row t / total, flat column t % total -> (window, column in it)
-    auto locate = [&](int t, int& w, int& m, int& kr) {
-        m = t / total;
-        int c = t - m * total;
-        w = 0;
-        for (;; ++w) {
-            if (win[w].off < 0) continue;
-            const int C4 = (win[w].khi - win[w].klo) * (GVM_COLS / 4);
-            if (c < C4) break;
-            c -= C4;
-        }
-        kr = 4 * c;
-    };
+    const int total = gvm_stage_columns(win, nwin);
     for (int t0 = threadIdx.x; t0 < M * total; t0 += 2 * NT) {
         float4 v[2];
 #pragma unroll
@@ -745,7 +755,7 @@ ES_DEV void gvm_stage_small(const GvLaunch& L, const GvmWin* win, int nwin, unsi
             v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (t < M * total) {
                 int w, m, kr;
-                locate(t, w, m, kr);
+                gvm_stage_item(win, total, t, w, m, kr);
                 const GvXSrc& x = L.xs[win[w].src];
                 const int k = win[w].klo * GVM_COLS + kr;
                 if (k < x.K) v[u] = gvm_x4(x, m, k, srinv);
@@ -756,7 +766,7 @@ ES_DEV void gvm_stage_small(const GvLaunch& L, const GvmWin* win, int nwin, unsi
             const int t = t0 + u * NT;
             if (t >= M * total) break;
             int w, m, kr;
-            locate(t, w, m, kr);
+            gvm_stage_item(win, total, t, w, m, kr);
             bf16* hi = reinterpret_cast<bf16*>(xsm + (size_t)win[w].off * 4) + (size_t)m * win[w].pw + kr;
             uint2 h, l;
             split2(v[u].x, v[u].y, h.x, l.x);

@@ -13,7 +13,10 @@
 //  * staged windows sit back to back within the budget, with a plane row
 //    stride of 64 mod 128 bytes (conflict-free fragment loads), and the
 //    device's rerun with the host's computed size as its budget stages the
-//    same windows at the same offsets.
+//    same windows at the same offsets;
+//  * the staging loops (gvm_stage_cursor's column walk and gvm_stage_item's
+//    item split, run here for every thread of a 256- and a 512-thread CTA)
+//    visit every (staged window, float4 column, activation row) exactly once.
 //
 // Exit status 0 when every check holds; the first failures go to stderr.
 #include <algorithm>
@@ -70,6 +73,45 @@ static std::vector<Stage> enumerate(const GvLaunch& L) {
                 for (int c = 0; c < L.segs[o.seg0 + s].nck; ++c) v.push_back({op, t, s, c});
     }
     return v;
+}
+
+static void check_staging(const GvLaunch& L, const GvmWin* win, int n, int cta) {
+    const int total = gvm_stage_columns(win, n), M = L.M;
+    std::vector<int> base(n + 1, 0);  // first float4 column of each window (0 columns if not staged)
+    for (int i = 0; i < n; ++i) base[i + 1] = base[i] + (win[i].off >= 0 ? (win[i].khi - win[i].klo) * (GVM_COLS / 4) : 0);
+    CHECK(base[n] == total, "cta %d: %d staged columns, counted %d", cta, total, base[n]);
+    std::vector<int> seen((size_t)total * M);
+    auto visit = [&](int w, int kr, int m, const char* how) {
+        const bool ok = w >= 0 && w < n && win[w].off >= 0 && kr % 4 == 0 && kr >= 0 &&
+                        kr < (win[w].khi - win[w].klo) * GVM_COLS && m >= 0 && m < M;
+        CHECK(ok, "cta %d (%s): window %d column %d row %d outside the staged windows", cta, how, w, kr, m);
+        if (ok) ++seen[(size_t)(base[w] + kr / 4) * M + m];
+    };
+    auto all_once = [&](const char* how, int nt) {
+        for (size_t i = 0; i < seen.size(); ++i)
+            CHECK(seen[i] == 1, "cta %d (%s, %d threads): item %zu visited %d times", cta, how, nt, i, seen[i]);
+        std::fill(seen.begin(), seen.end(), 0);
+    };
+    for (int nt : {256, 512}) {
+        for (int tid = 0; tid < nt; ++tid) {
+            int w = 0, wbase = 0;
+            for (int c = tid; c < total; c += nt) {
+                gvm_stage_cursor(win, c, w, wbase);
+                for (int m = 0; m < M; ++m) visit(w, (c - wbase) * 4, m, "columns");
+            }
+        }
+        all_once("columns", nt);
+        for (int tid = 0; tid < nt; ++tid)
+            for (int t0 = tid; t0 < M * total; t0 += 2 * nt)
+                for (int u = 0; u < 2; ++u) {
+                    const int t = t0 + u * nt;
+                    if (t >= M * total) break;
+                    int w, m, kr;
+                    gvm_stage_item(win, total, t, w, m, kr);
+                    visit(w, kr, m, "items");
+                }
+        all_once("items", nt);
+    }
 }
 
 static void check_launch(const GvLaunch& L) {
@@ -143,6 +185,7 @@ static void check_launch(const GvLaunch& L) {
                 CHECK(wb[i].off == -1, "cta %d: window %d of %d words staged past the budget", cta, i, words);
             }
         }
+        check_staging(L, wb, nb, cta);
         used_at_max[cta] = ub;
         need = std::max(need, ub);
     }

@@ -6,7 +6,11 @@ kernel itself runs) over 400 random launches: ragged widths, 1-8 activation
 rows, 1-8 ops of 1-3 segments, the 8- and 16-warp layouts and small grids.
 It checks stage coverage and order, window coverage, disjointness, budget
 and plane stride, and that the device's rerun of the window function with
-the host's computed size stages the same windows. Compiled with nvcc; no GPU.
+the host's computed size stages the same windows.  It also runs the
+staging loops' index helpers (the column walk's forward-only window cursor
+and the small-window item split) for every thread of a 256- and a
+512-thread CTA and checks that each staged (window, float4 column, row) is
+visited exactly once.  Compiled with nvcc; no GPU.
 """
 import os
 import subprocess
