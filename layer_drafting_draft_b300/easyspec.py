@@ -161,6 +161,7 @@ class EasySpec:
         self._wd, self._wb = _WeightTable(draft_w), _WeightTable(base_w)
         self.stream = stream if stream is not None else torch.cuda.current_stream()
         self.V = draft_shape["vocab"]
+        self._shapes = (dict(draft_shape), dict(base_shape))
         self._gs = None
         cfg = es_config(_shape(draft_shape, dtype), _shape(base_shape, dtype), max_batch, max_seq,
                         max_gamma, mode, None, 0, C.c_void_p(self.stream.cuda_stream))
@@ -252,6 +253,12 @@ class EasySpec:
 
     def es_read_kv(self, which: int, layer: int, seq: int, n: int, kv_heads: int, head_dim: int):
         import numpy as np
+        # the library writes n x (the model's kv heads) x (its head size)
+        # floats per array: the host buffers must have exactly that size
+        s = self._shapes[1 if which else 0]
+        if (kv_heads, head_dim) != (s["n_kv_heads"], s["head_dim"]):
+            raise ValueError(f"es_read_kv: the {'base' if which else 'draft'} model has "
+                             f"{s['n_kv_heads']} kv heads of {s['head_dim']}, not {kv_heads} of {head_dim}")
         k = np.zeros((n, kv_heads, head_dim), np.float32)
         v = np.zeros_like(k)
         self._check(self._lib.es_read_kv(self.ctx, which, layer, seq, n,
@@ -331,7 +338,16 @@ def es_accept_resample_noalloc(p: torch.Tensor, q: torch.Tensor, d: torch.Tensor
 
 def es_sample(w: torch.Tensor, u: torch.Tensor):
     """Quantised categorical draw per row of w [B,V] f32 with draws u [B]."""
+    if not isinstance(w, torch.Tensor) or w.dim() != 2:
+        raise ValueError("w must be a [B, V] tensor")
     B, V = w.shape
+    # the kernel reads w and u as dense device arrays of these sizes
+    for name, t, dt, shp in (("w", w, torch.float32, (B, V)), ("u", u, torch.int64, (B,))):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.device != w.device:
+            raise ValueError(f"{name} must be a CUDA tensor on w's device")
+        if t.dtype != dt or tuple(t.shape) != shp or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {dt} tensor of shape {shp}, "
+                             f"got {t.dtype} {tuple(t.shape)}")
     idx = torch.empty(B, dtype=torch.int32, device=w.device)
     st = lib().es_sample(_ptr(w), _ptr(u), B, V, _ptr(idx), torch.cuda.current_stream().cuda_stream)
     if st != ES_OK:
